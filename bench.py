@@ -1,0 +1,515 @@
+"""Benchmark: credit-assignment timesteps/s of GAE with truncation bootstrapping on
+[4096, 1024] fp32 rollouts, and the fraction of the GB300 HBM roofline it reaches.
+
+One step = one fused GAE launch (load -> operand build -> segmented reverse scan ->
+advantages and returns written once) over one [4096, 1024] batch that is already in
+HBM. Batches rotate over several distinct seeded input sets whose total size exceeds
+the L2 cache, so no step reads another step's inputs from L2. The timed steps are
+replayed from CUDA graphs so that host launch overhead does not idle the GPU.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rlca|reference]
+With --impl reference the fp64 CPU oracle is timed instead, on a bounded sample of the
+same workload, on this host's cores. Under torchrun every rank runs its own batch
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_rollouts as sr  # noqa: E402
+
+METRIC = "credit-assignment timesteps/sec at [4096,1024] fp32; % of GB300 HBM roofline"
+UNIT = "timesteps/s"
+N_ENVS, SEQ_LEN = 4096, 1024
+WORKLOAD = "GAE with truncation bootstrapping, fp32, num_envs=4096, seq_len=1024"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+# DRAM bytes per launch measured by ncu for the GAE [4096,1024] kernel, keyed by a hash of
+# the kernel sources at the time of the capture; null once the kernels change.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "segmented_associative_scan_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def algorithmic_bytes(est: str, ro) -> int:
+    """Minimal HBM bytes of one launch: every input element the estimator needs read once
+    (truncation values only where a step is truncated and not terminated; per-env
+    bootstrap values once) and every output written once."""
+    n = ro.N * ro.T
+    f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4}[est]
+    outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1}[est]
+    b = n * (4 * f32_in + 1 + 4 * outs)
+    if ro.truncated is not None:
+        b += n + 4 * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
+    if ro.bootstrap is not None:
+        b += 4 * ro.N
+    return b
+
+
+def workload_inputs(est: str, N: int, T: int, seed: int):
+    """The seeded workload each estimator is quoted on, at [N, T]."""
+    if est == "gae":
+        return sr.gae_trunc(N=N, T=T, seed=seed)
+    if est in ("return", "td_lambda"):
+        return sr.return_td(N=N, T=T, seed=seed)
+    if est == "vtrace":
+        return sr.vtrace(N=N, T=T, seed=seed)
+    return sr.retrace(N=N, T=T, seed=seed)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 100 ms, in the
+    background; `summary(t0, t1)` keeps the samples taken inside [t0, t1]."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append(dict(t=time.time(), sm=float(parts[2]),
+                                         sm_max=float(parts[3]),
+                                         reasons=[name for name, v in zip(
+                                             ("hw_slowdown", "hw_thermal_slowdown",
+                                              "sw_thermal_slowdown", "sw_power_cap"),
+                                             parts[5:9]) if v.lower() == "active"]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        window = "timed region"
+        if not inside:
+            inside = self.samples
+            window = "whole run (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "nvidia-smi unavailable"}
+        reasons = sorted({r for s in inside for r in s["reasons"]})
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["sm_max"] for s in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class DeviceSet:
+    """One batch resident in HBM plus its output buffers."""
+
+    def __init__(self, ro, device):
+        import torch
+        self.ro = ro
+        t = lambda a: None if a is None else torch.from_numpy(a).to(device)
+        self.reward, self.value = t(ro.reward), t(ro.value)
+        self.terminated, self.truncated = t(ro.terminated), t(ro.truncated)
+        self.trunc_value, self.bootstrap = t(ro.trunc_value), t(ro.bootstrap)
+        self.log_rho, self.q_taken, self.expected_q, self.rho = (
+            t(ro.log_rho), t(ro.q_taken), t(ro.expected_q), t(ro.rho))
+        z = lambda: torch.empty((ro.N, ro.T), dtype=torch.float32, device=device)
+        self.out0, self.out1 = z(), z()
+
+    def clone(self):
+        import torch
+        c = object.__new__(DeviceSet)
+        for k, v in self.__dict__.items():
+            setattr(c, k, v.clone() if isinstance(v, torch.Tensor) else v)
+        return c
+
+
+def launch(rlca, est, s, params):
+    fl = dict(terminated=s.terminated, truncated=s.truncated,
+              trunc_value=s.trunc_value if s.truncated is not None else None)
+    g = params["gamma"]
+    if est == "gae":
+        rlca.rlca_gae(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
+                      lam=params["lam"], advantages=s.out0, returns=s.out1)
+    elif est == "return":
+        rlca.rlca_discounted_return(s.reward, **fl, bootstrap=s.bootstrap, gamma=g,
+                                    returns=s.out0)
+    elif est == "td_lambda":
+        rlca.rlca_td_lambda(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
+                            lam=params["lam"], targets=s.out0)
+    elif est == "vtrace":
+        rlca.rlca_vtrace(s.reward, s.value, s.log_rho, **fl, bootstrap=s.bootstrap, gamma=g,
+                         lam=params["lam"], rho_bar=params["rho_bar"],
+                         c_bar=params["c_bar"], pg_rho_bar=params["pg_rho_bar"],
+                         vs=s.out0, pg_advantages=s.out1)
+    else:
+        rlca.rlca_retrace(s.reward, s.q_taken, s.expected_q, s.rho, **fl,
+                          bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0)
+
+
+def est_params(est, ro):
+    p = dict(ro.params)
+    if est == "td_lambda":
+        p["lam"] = 0.9
+    return p
+
+
+def capture(torch, rlca, est, sets, params, n_steps, first=0):
+    """A CUDA graph of n_steps launches, step i on input set (first + i) % len(sets)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_steps):
+            launch(rlca, est, sets[(first + i) % len(sets)], params)
+    return g
+
+
+def timed_replay(torch, graphs):
+    """Replay graphs between two CUDA events on the current stream; ms elapsed."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def n_sets_for(bytes_per_set):
+    return max(3, int(np.ceil(2.5 * L2_BYTES / bytes_per_set)))
+
+
+def per_estimator_roofline(torch, rlca, device, peak):
+    """Each estimator alone at [4096, 1024] on its own workload's distributions."""
+    out = {}
+    for est in ("return", "td_lambda", "gae", "vtrace", "retrace"):
+        ro = workload_inputs(est, N_ENVS, SEQ_LEN, seed=100)
+        params = est_params(est, ro)
+        nbytes = algorithmic_bytes(est, ro)
+        base = DeviceSet(ro, device)
+        sets = [base] + [base.clone() for _ in range(n_sets_for(nbytes) - 1)]
+        for i in range(3):
+            launch(rlca, est, sets[i % len(sets)], params)
+        G = 10 * len(sets)
+        g = capture(torch, rlca, est, sets, params, G)
+        g.replay()
+        reps = max(1, 300 // G)
+        ms = timed_replay(torch, [g] * reps)
+        us = 1000.0 * ms / (G * reps)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[est] = {"us_per_launch": round(us, 3), "algorithmic_bytes": nbytes,
+                    "bytes_per_step": round(nbytes / (ro.N * ro.T), 3),
+                    "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "frac_of_8tbs": round(gbs / 8000.0, 4),
+                    "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1)}
+        del sets, base, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def e2e_run(torch, rlca, ro, device, n_steps):
+    """Public API end to end: pinned host -> device copies of the step's inputs, the
+    fused GAE call, device -> pinned host copies of advantages and returns."""
+    names = ("reward", "value", "terminated", "truncated", "trunc_value", "bootstrap")
+    host = {k: torch.from_numpy(getattr(ro, k)).pin_memory() for k in names}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    adv_h = torch.empty((ro.N, ro.T), dtype=torch.float32).pin_memory()
+    ret_h = torch.empty_like(adv_h).pin_memory()
+    params = ro.params
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = 2 * adv_h.numel() * 4
+
+    def step():
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        adv, ret = rlca.rlca_gae(dev["reward"], dev["value"], dev["terminated"],
+                                 dev["truncated"], dev["trunc_value"], dev["bootstrap"],
+                                 gamma=params["gamma"], lam=params["lam"])
+        adv_h.copy_(adv, non_blocking=True)
+        ret_h.copy_(ret, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(ro.N * ro.T * n_steps / (ms * 1e-3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
+            "ms_per_step": round(ms / n_steps, 4)}
+
+
+def cpu_baseline(ro, seconds):
+    """The fp64 oracle as it stands, single thread, on the full batch, repeated for about
+    `seconds` of CPU time."""
+    import oracle
+    oracle.build()
+    p = ro.params
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gae(ro.reward, ro.value, ro.terminated, ro.truncated, ro.trunc_value,
+                   ro.bootstrap, gamma=p["gamma"], lam=p["lam"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(reps * ro.N * ro.T / el, 1), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"full [{ro.N},{ro.T}] GAE batch (seed 0), {reps} passes, "
+                      f"{el:.1f} s, single thread, fp64 C reverse loop"}
+
+
+def gpu_arm(args, rank, world, local_rank, dist):
+    import torch
+
+    import segmented_associative_scan_gb300 as rlca
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    rlca.lib()
+    peak, peak_src = measured_peaks()
+
+    # Distinct seeded batches, resident in HBM, rotating so their total exceeds L2.
+    ro0 = workload_inputs("gae", N_ENVS, SEQ_LEN, seed=1000 * rank)
+    nbytes = algorithmic_bytes("gae", ro0)
+    n_sets = n_sets_for(nbytes)
+    sets = [DeviceSet(ro0, device)]
+    for i in range(1, n_sets):
+        sets.append(DeviceSet(workload_inputs("gae", N_ENVS, SEQ_LEN, 1000 * rank + i), device))
+    params = est_params("gae", ro0)
+    step_bytes = [algorithmic_bytes("gae", s.ro) for s in sets]
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        launch(rlca, "gae", sets[i % n_sets], params)
+    torch.cuda.synchronize()
+    G = n_sets * max(1, 96 // n_sets)
+    graphs = [capture(torch, rlca, "gae", sets, params, G)] * (K // G)
+    if K % G:
+        graphs.append(capture(torch, rlca, "gae", sets, params, K % G))
+    graphs[0].replay()
+    torch.cuda.synchronize()
+    kernel_bytes_per_step = sum(step_bytes[i % n_sets] for i in range(K)) / K
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    # Hold the GPU busy for ~0.5 s before timing so the clock samples see it under load.
+    soak_end = time.time() + (0.0 if args.profile else 0.5)
+    while time.time() < soak_end:
+        graphs[0].replay()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = timed_replay(torch, graphs)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    if rank != 0:
+        return None
+
+    launch_us = 1000.0 * ms / K
+    achieved = kernel_bytes_per_step / (launch_us * 1e-6) / 1e9
+    value = world * N_ENVS * SEQ_LEN * K / (ms_max * 1e-3)
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(src_hash)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded rollouts with the workload's distributions (no dataset)",
+        "config": {
+            "workload": WORKLOAD, "estimator": "gae", "num_envs": N_ENVS,
+            "seq_len": SEQ_LEN, "gamma": params["gamma"], "lambda": params["lam"],
+            "input_sets": n_sets,
+            "l2": f"inputs larger than L2: {n_sets} distinct batches of "
+                  f"{nbytes / 1e6:.1f} MB rotate ({n_sets * nbytes / 1e6:.0f} MB > "
+                  f"{L2_BYTES / 1e6:.0f} MB L2)",
+            "timing": f"CUDA graphs of {G} launches replayed between CUDA events on the "
+                      "launch stream; one fused kernel launch per step",
+            "parallelism": f"replicas{world}: each GPU its own batch, no collective"},
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": "credit_scan_kernel<GAE, whole-row tiles>",
+            "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),
+            "launch_us": round(launch_us, 3), "peak_source": peak_src,
+            "frac_of_8tbs": round(achieved / 8000.0, 4), "kernel_source": src_hash},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        result["e2e"] = e2e_run(torch, rlca, ro0, device, min(K, args.e2e_steps))
+    del graphs, sets
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_estimators:
+        result["estimators"] = per_estimator_roofline(torch, rlca, device, peak)
+    if world == 1 and args.cpu_seconds > 0:
+        result["cpu_baseline"] = cpu_baseline(ro0, args.cpu_seconds)
+    return result
+
+
+# --------------------------------------------------------------------- reference arm
+
+def reference_arm(args):
+    """The fp64 CPU oracle as it stands, on this host's cores (one thread), each step a
+    bounded sample (the first rows) of the same [4096, 1024] GAE workload."""
+    import oracle
+    oracle.build()
+    ro = workload_inputs("gae", N_ENVS, SEQ_LEN, seed=0)
+    p = ro.params
+
+    def run(rows):
+        oracle.gae(ro.reward[:rows], ro.value[:rows], ro.terminated[:rows],
+                   ro.truncated[:rows], ro.trunc_value[:rows], ro.bootstrap[:rows],
+                   gamma=p["gamma"], lam=p["lam"])
+
+    t0 = time.perf_counter()
+    run(256)
+    per_row = (time.perf_counter() - t0) / 256
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(N_ENVS, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        run(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(rows)
+    el = time.perf_counter() - t0
+    value = rows * SEQ_LEN * args.steps / el
+    sample = (f"first {rows} of {N_ENVS} envs x {SEQ_LEN} steps per step, "
+              f"single thread, fp64 C reverse loop")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * el / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded rollouts with the workload's distributions (no dataset)",
+        "config": {"workload": WORKLOAD, "estimator": "gae", "num_envs": N_ENVS,
+                   "seq_len": SEQ_LEN, "sample_envs": rows},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("rlca", "reference"), default="rlca")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-estimators", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for profilers: no clock soak, e2e, per-estimator table "
+                         "or CPU baseline")
+    args = ap.parse_args()
+    if args.profile:
+        args.no_e2e = args.no_estimators = True
+        args.cpu_seconds = 0.0
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    try:
+        res = gpu_arm(args, rank, world, local_rank, dist)
+    finally:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * rlca.h - C ABI of librlca: reinforcement-learning credit assignment on one GB300
+ * (sm_103a), each estimator computed as one fused, segmented, reverse affine scan.
+ *
+ * Source: "rl-triton: High-Performance Triton GPU Kernels for Reinforcement Learning
+ * Credit Assignment" (technical summary).
+ *   - Problem statement: credit-assignment quantities (advantages, value targets,
+ *     returns) over [num_envs, seq_len] tensors of rewards, values and done flags.
+ *   - Method section 1: every estimator is the first-order recurrence
+ *     A_t = alpha_t + beta_t * A_{t+1}, solved as an associative scan over the pairs
+ *     (alpha_t, beta_t) with (aB, bB) (+) (aA, bA) = (aB + bB * aA, bA * bB).
+ *   - Method section 2: the pairs are built on chip from the raw inputs; inputs are
+ *     read from HBM once and outputs written once.
+ *   - Method section 3: a terminated step has successor value 0; a truncated step
+ *     bootstraps from a supplied value; the last step of the window (t = T-1)
+ *     bootstraps from a supplied per-env value, counted exactly once.
+ *
+ * Common conventions (all entry points)
+ *   Layout    Every per-step array is row-major [N, ld] in device memory: row n holds
+ *             env n, steps t = 0..T-1 in columns 0..T-1 (T contiguous), ld >= T.
+ *             Outputs use the same layout and ld; their columns T..ld-1 are not
+ *             written. Data are float32; flags are uint8 (0 = clear, nonzero = set;
+ *             a torch.bool tensor qualifies). Per-env bootstrap values are float32 [N].
+ *   Flags     terminated[n,t]: the episode ended at step t (successor value 0, no credit
+ *             from t+1). truncated[n,t] (nullable = none truncated): the episode was
+ *             cut at t; its successor value is trunc_value[n,t], which is read only
+ *             where truncated is set. If both are set, termination wins. At t = T-1 the
+ *             successor value is bootstrap[n] (nullable = 0) unless the step is
+ *             terminated or truncated.
+ *   Stream    `stream` is a cudaStream_t (NULL = the legacy default stream) of the
+ *             current device; all work is enqueued on it, asynchronously. Pointers must
+ *             belong to the current device.
+ *   Ownership The caller owns every buffer. The library never allocates or frees
+ *             memory, never synchronises, and never changes the current device. Inputs
+ *             are read only. Outputs must not overlap any input or each other.
+ *   Errors    0 = RLCA_OK. A negative code means nothing was enqueued, except
+ *             RLCA_ERR_LAUNCH (the launch itself failed; cudaGetLastError is cleared).
+ *             N == 0 or T == 0 is a valid empty problem: RLCA_OK, nothing enqueued.
+ *   Precision fp32 arithmetic, round to nearest, no fast-math; exp is the CUDA libm
+ *             expf. The scan reassociates the recurrence, so results differ from a
+ *             sequential loop by rounding only.
+ */
+#ifndef RLCA_H
+#define RLCA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum rlca_status {
+    RLCA_OK = 0,
+    RLCA_ERR_NULL = -1,      /* a required pointer is NULL */
+    RLCA_ERR_SHAPE = -2,     /* N < 0, T < 0, ld < T, T > RLCA_MAX_T, or N*ld overflows */
+    RLCA_ERR_PARAM = -3,     /* gamma < 0 or not finite; lambda outside [0,1]; a clip <= 0 or NaN */
+    RLCA_ERR_ALIAS = -4,     /* an output overlaps an input or another output */
+    RLCA_ERR_WORKSPACE = -5, /* workspace too small or misaligned */
+    RLCA_ERR_LAUNCH = -6,    /* the CUDA launch failed */
+    RLCA_ERR_TIMEOUT = -7    /* a bounded cross-block wait gave up (see rlca_workspace_check) */
+};
+
+/* Largest supported seq_len. */
+#define RLCA_MAX_T (1 << 30)
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int rlca_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+const char *rlca_status_string(int status);
+
+/*
+ * Discounted return G_t = r_t + gamma * G_{t+1} inside an episode, and
+ * G_t = r_t + gamma * (successor value) at its last step.
+ * Scan form: alpha_t = r_t (+ gamma * successor value at the episode's last step),
+ * beta_t = gamma.
+ * Inputs: reward, terminated [N,ld]; truncated, trunc_value [N,ld] (nullable, together);
+ * bootstrap [N] (nullable). Output: returns [N,ld].
+ */
+int rlca_discounted_return(const float *reward, const uint8_t *terminated,
+                           const uint8_t *truncated, const float *trunc_value,
+                           const float *bootstrap, float gamma, int64_t N, int64_t T,
+                           int64_t ld, float *returns, void *stream);
+
+/*
+ * TD(lambda) lambda-returns (Sutton & Barto):
+ * G_t = r_t + gamma * ((1 - lambda) V_{t+1} + lambda G_{t+1}) inside an episode,
+ * G_t = r_t + gamma * (successor value) at its last step.
+ * Scan form: alpha_t = r_t + gamma (1 - lambda) V_{t+1}, beta_t = gamma lambda.
+ * Inputs as rlca_discounted_return plus value [N,ld]. Output: targets [N,ld].
+ */
+int rlca_td_lambda(const float *reward, const float *value, const uint8_t *terminated,
+                   const uint8_t *truncated, const float *trunc_value,
+                   const float *bootstrap, float gamma, float lambda, int64_t N,
+                   int64_t T, int64_t ld, float *targets, void *stream);
+
+/*
+ * GAE (Schulman et al. 2016): delta_t = r_t + gamma V(s_{t+1}) - V_t,
+ * A_t = delta_t + gamma lambda A_{t+1} inside an episode (A_t = delta_t at its last
+ * step); returns_t = A_t + V_t. V(s_{t+1}) is V_{t+1} inside an episode and the
+ * successor value at its last step.
+ * Scan form: alpha_t = delta_t, beta_t = gamma lambda.
+ * Outputs: advantages [N,ld]; returns [N,ld] (nullable: not written).
+ */
+int rlca_gae(const float *reward, const float *value, const uint8_t *terminated,
+             const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+             float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+             float *advantages, float *returns, void *stream);
+
+/*
+ * V-trace (Espeholt et al. 2018, IMPALA), from log importance ratios log_rho [N,ld]:
+ * rho_t = exp(log_rho_t), rho_hat_t = min(rho_bar, rho_t), c_t = lambda min(c_bar, rho_t),
+ * vs_t - V_t = rho_hat_t (r_t + gamma V(s_{t+1}) - V_t) + gamma c_t (vs_{t+1} - V_{t+1})
+ * inside an episode (last term absent at its last step);
+ * pg_t = min(pg_rho_bar, rho_t) (r_t + gamma q_{t+1} - V_t), q_{t+1} = vs_{t+1} inside an
+ * episode, the successor value at its last step.
+ * Scan form: A_t = vs_t - V_t, alpha_t = rho_hat_t delta_t, beta_t = gamma c_t.
+ * Outputs: vs [N,ld]; pg_advantages [N,ld] (nullable: not written).
+ */
+int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
+                const uint8_t *terminated, const uint8_t *truncated,
+                const float *trunc_value, const float *bootstrap, float gamma,
+                float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream);
+
+/*
+ * Retrace(lambda) (Munos et al. 2016), from importance ratios rho [N,ld],
+ * Q(s_t, a_t) = q_taken [N,ld] and E_pi Q(s_t, .) = expected_q [N,ld]:
+ * c_t = lambda min(1, rho_t),
+ * Q^ret_t = r_t + gamma E_pi Q(s_{t+1},.) + gamma c_{t+1} (Q^ret_{t+1} - Q(s_{t+1},a_{t+1}))
+ * inside an episode (last term absent at its last step). At the episode's last step
+ * E_pi Q(s_{t+1},.) is 0 (terminated), trunc_value (truncated) or bootstrap_ev[n]
+ * (window end; nullable = 0).
+ * Scan form: A_t = Q^ret_t - Q_t, alpha_t = r_t + gamma E_pi Q(s_{t+1},.) - Q_t,
+ * beta_t = gamma c_{t+1}. Output: q_ret [N,ld].
+ */
+int rlca_retrace(const float *reward, const float *q_taken, const float *expected_q,
+                 const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+                 const float *trunc_value, const float *bootstrap_ev, float gamma,
+                 float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                 void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RLCA_H */

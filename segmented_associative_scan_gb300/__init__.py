@@ -1,0 +1,214 @@
+"""Python binding of librlca: RL credit assignment as fused segmented reverse affine
+scans on one GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels of
+``librlca.so``; PyTorch supplies device memory and the current stream. There is no CPU
+fallback: if the library is not built, every call raises.
+
+The functions carry the names of the C entry points (``include/rlca.h``) and take
+torch tensors:
+  - per-step tensors: CUDA, 2-D [N, T], unit stride along T, all with the same row
+    stride; float32 data, uint8 or bool flags;
+  - per-env bootstrap values: CUDA float32 [N] (optional);
+  - outputs are allocated (same row stride as the inputs) unless passed in.
+Work is enqueued on ``torch.cuda.current_stream()``; nothing synchronises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librlca.so")
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+SIGNATURES = {
+    "rlca_version": ([], ctypes.c_int),
+    "rlca_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "rlca_discounted_return": ([_P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _P, _P],
+                               ctypes.c_int),
+    "rlca_td_lambda": ([_P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P],
+                       ctypes.c_int),
+    "rlca_gae": ([_P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P, _P],
+                 ctypes.c_int),
+    "rlca_vtrace": ([_P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _F, _I64, _I64, _I64, _P,
+                     _P, _P], ctypes.c_int),
+    "rlca_retrace": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P],
+                     ctypes.c_int),
+}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile librlca.so in-tree (nvcc, sm_103a)."""
+    from . import buildlib as _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library with argument types set. Raises if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "segmented_associative_scan_gb300.build()")
+        cdll = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(cdll, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = cdll
+    return _lib
+
+
+class RlcaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib().rlca_status_string(status).decode()} (status {status})")
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise RlcaError(fn, status)
+
+
+class _Rows:
+    """Shape/stride bookkeeping shared by the per-step tensors of one call."""
+
+    def __init__(self, ref: torch.Tensor):
+        if ref.dim() != 2:
+            raise ValueError("per-step tensors must be 2-D [num_envs, seq_len]")
+        self.N, self.T = ref.shape
+        self.ld = ref.stride(0) if self.N > 1 else max(ref.stride(0), self.T)
+        self.device = ref.device
+
+    def ptr(self, t, name, dtypes, optional=False):
+        if t is None:
+            if optional:
+                return None
+            raise ValueError(f"{name} is required")
+        if not t.is_cuda or t.device != self.device:
+            raise ValueError(f"{name} must be on {self.device}")
+        if t.dtype not in dtypes:
+            raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+        if tuple(t.shape) != (self.N, self.T):
+            raise ValueError(f"{name}: shape {tuple(t.shape)} != {(self.N, self.T)}")
+        if self.T > 1 and t.stride(1) != 1:
+            raise ValueError(f"{name}: steps must be contiguous (stride(1) == 1)")
+        if self.N > 1 and t.stride(0) != self.ld:
+            raise ValueError(f"{name}: row stride {t.stride(0)} != {self.ld}")
+        return t.data_ptr() or None
+
+    def vec_ptr(self, t, name):
+        if t is None:
+            return None
+        if not t.is_cuda or t.dtype != torch.float32 or t.dim() != 1 or t.shape[0] != self.N:
+            raise ValueError(f"{name} must be a CUDA float32 [{self.N}] tensor")
+        if self.N > 1 and t.stride(0) != 1:
+            raise ValueError(f"{name} must be contiguous")
+        return t.data_ptr() or None
+
+    def out(self, t, name):
+        if t is None:
+            buf = torch.empty((self.N, max(self.ld, self.T)), dtype=torch.float32,
+                              device=self.device)
+            t = buf[:, :self.T]
+        self.ptr(t, name, (torch.float32,))
+        return t
+
+
+_F32 = (torch.float32,)
+_FLAG = (torch.uint8, torch.bool)
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def rlca_discounted_return(reward, terminated, truncated=None, trunc_value=None,
+                           bootstrap=None, gamma=0.99, returns=None):
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(terminated, "terminated", _FLAG),
+            g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    returns = g.out(returns, "returns")
+    _check("rlca_discounted_return", lib().rlca_discounted_return(
+        *args, gamma, g.N, g.T, g.ld, returns.data_ptr() or None, _stream(g.device)))
+    return returns
+
+
+def rlca_td_lambda(reward, value, terminated, truncated=None, trunc_value=None,
+                   bootstrap=None, gamma=0.99, lam=0.95, targets=None):
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+            g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    targets = g.out(targets, "targets")
+    _check("rlca_td_lambda", lib().rlca_td_lambda(
+        *args, gamma, lam, g.N, g.T, g.ld, targets.data_ptr() or None, _stream(g.device)))
+    return targets
+
+
+def rlca_gae(reward, value, terminated, truncated=None, trunc_value=None, bootstrap=None,
+             gamma=0.99, lam=0.95, advantages=None, returns=None, want_returns=True):
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+            g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    advantages = g.out(advantages, "advantages")
+    returns = g.out(returns, "returns") if (want_returns or returns is not None) else None
+    _check("rlca_gae", lib().rlca_gae(
+        *args, gamma, lam, g.N, g.T, g.ld, advantages.data_ptr() or None,
+        returns.data_ptr() or None if returns is not None else None, _stream(g.device)))
+    return advantages, returns
+
+
+def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=None,
+                bootstrap=None, gamma=0.99, lam=1.0, rho_bar=1.0, c_bar=1.0,
+                pg_rho_bar=None, vs=None, pg_advantages=None, want_pg=True):
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+            g.ptr(log_rho, "log_rho", _F32), g.ptr(terminated, "terminated", _FLAG),
+            g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    vs = g.out(vs, "vs")
+    pg = g.out(pg_advantages, "pg_advantages") if (want_pg or pg_advantages is not None) \
+        else None
+    if pg_rho_bar is None:
+        pg_rho_bar = rho_bar
+    _check("rlca_vtrace", lib().rlca_vtrace(
+        *args, gamma, lam, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld,
+        vs.data_ptr() or None, pg.data_ptr() or None if pg is not None else None,
+        _stream(g.device)))
+    return vs, pg
+
+
+def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
+                 trunc_value=None, bootstrap_ev=None, gamma=0.99, lam=0.95, q_ret=None):
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(q_taken, "q_taken", _F32),
+            g.ptr(expected_q, "expected_q", _F32), g.ptr(rho, "rho", _F32),
+            g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap_ev, "bootstrap_ev"))
+    q_ret = g.out(q_ret, "q_ret")
+    _check("rlca_retrace", lib().rlca_retrace(
+        *args, gamma, lam, g.N, g.T, g.ld, q_ret.data_ptr() or None, _stream(g.device)))
+    return q_ret
+
+
+# Short names.
+discounted_return = rlca_discounted_return
+td_lambda = rlca_td_lambda
+gae = rlca_gae
+vtrace = rlca_vtrace
+retrace = rlca_retrace

@@ -1,0 +1,217 @@
+// C ABI of librlca (declared in include/rlca.h): argument validation, then one fused
+// kernel launch on the caller's stream. No allocation, no synchronisation, no change
+// of the current device.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/rlca.h"
+#include "launch.cuh"
+
+namespace {
+
+using rlca::Params;
+
+struct Range {
+    uintptr_t lo, hi;
+};
+
+// Bytes spanned by a [N, ld] array of which the first T columns are used.
+Range span(const void *p, int64_t N, int64_t T, int64_t ld, size_t elem)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + (uintptr_t)(((N - 1) * ld + T) * (int64_t)elem)};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape check shared by every entry point. Sets *empty for N == 0 or T == 0.
+int check_shape(int64_t N, int64_t T, int64_t ld, bool *empty)
+{
+    if (N < 0 || T < 0 || ld < T || T > RLCA_MAX_T) return RLCA_ERR_SHAPE;
+    *empty = (N == 0 || T == 0);
+    if (*empty) return RLCA_OK;
+    if (ld > INT64_MAX / 8 / N) return RLCA_ERR_SHAPE;
+    return RLCA_OK;
+}
+
+bool bad_gamma(float g) { return !std::isfinite(g) || g < 0.f; }
+bool bad_lambda(float l) { return !(l >= 0.f && l <= 1.f); }
+bool bad_clip(float c) { return std::isnan(c) || !(c > 0.f); }
+
+// Common validation of the optional/required inputs and the outputs, then launch.
+// `f32_in` are the required float inputs read with vector loads, `outs` the outputs.
+template <typename LaunchFn>
+int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *const *outs,
+                        int n_out, LaunchFn launch, void *stream)
+{
+    // An empty problem is valid whatever the pointers (an empty tensor may have none).
+    bool empty = false;
+    int st = check_shape(p.N, p.T, p.ld, &empty);
+    if (st != RLCA_OK || empty) return st;
+
+    for (int i = 0; i < n_in; ++i)
+        if (!f32_in[i]) return RLCA_ERR_NULL;
+    if (!p.term || !outs[0]) return RLCA_ERR_NULL;
+    if (p.trunc && !p.trunc_value) return RLCA_ERR_NULL;
+
+    // Outputs may overlap neither an input nor each other.
+    Range in_ranges[8];
+    int k = 0;
+    for (int i = 0; i < n_in; ++i) in_ranges[k++] = span(f32_in[i], p.N, p.T, p.ld, 4);
+    in_ranges[k++] = span(p.term, p.N, p.T, p.ld, 1);
+    if (p.trunc) {
+        in_ranges[k++] = span(p.trunc, p.N, p.T, p.ld, 1);
+        in_ranges[k++] = span(p.trunc_value, p.N, p.T, p.ld, 4);
+    }
+    if (p.boot) in_ranges[k++] = span(p.boot, 1, p.N, p.N, 4);
+    for (int o = 0; o < n_out; ++o) {
+        if (!outs[o]) continue;
+        const Range ro = span(outs[o], p.N, p.T, p.ld, 4);
+        for (int i = 0; i < k; ++i)
+            if (overlaps(ro, in_ranges[i])) return RLCA_ERR_ALIAS;
+        for (int q = o + 1; q < n_out; ++q)
+            if (outs[q] && overlaps(ro, span(outs[q], p.N, p.T, p.ld, 4))) return RLCA_ERR_ALIAS;
+    }
+
+    // 128-bit loads/stores need 16-byte aligned rows: ld % 4 == 0 and aligned bases.
+    bool vec = (p.ld % 4) == 0 && aligned(p.term, 4) && (!p.trunc || aligned(p.trunc, 4));
+    for (int i = 0; i < n_in; ++i) vec = vec && aligned(f32_in[i], 16);
+    for (int o = 0; o < n_out; ++o) vec = vec && (!outs[o] || aligned(outs[o], 16));
+
+    const cudaError_t err = launch(p, vec, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? RLCA_OK : RLCA_ERR_LAUNCH;
+}
+
+Params base_params(const float *reward, const uint8_t *term, const uint8_t *trunc,
+                   const float *tv, const float *boot, float gamma, float lambda, int64_t N,
+                   int64_t T, int64_t ld)
+{
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.reward = reward;
+    p.term = term;
+    p.trunc = trunc;
+    p.trunc_value = trunc ? tv : nullptr;
+    p.boot = boot;
+    p.N = N;
+    p.T = (T < 0 || T > RLCA_MAX_T) ? -1 : (int)T;  // out of range -> RLCA_ERR_SHAPE
+    p.ld = ld;
+    p.gamma = gamma;
+    p.lambda = lambda;
+    p.gamma_lambda = gamma * lambda;
+    p.gamma_one_m_lambda = gamma * (1.f - lambda);
+    p.rho_bar = p.c_bar = p.pg_rho_bar = 1.f;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rlca_version(void) { return 100; }
+
+const char *rlca_status_string(int status)
+{
+    switch (status) {
+    case RLCA_OK: return "ok";
+    case RLCA_ERR_NULL: return "a required pointer is NULL";
+    case RLCA_ERR_SHAPE: return "invalid shape (N < 0, T < 0, ld < T, T too large, or N*ld overflows)";
+    case RLCA_ERR_PARAM: return "invalid parameter (gamma < 0 or not finite, lambda outside [0,1], or a clip <= 0)";
+    case RLCA_ERR_ALIAS: return "an output overlaps an input or another output";
+    case RLCA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case RLCA_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case RLCA_ERR_TIMEOUT: return "a bounded cross-block wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int rlca_discounted_return(const float *reward, const uint8_t *terminated,
+                           const uint8_t *truncated, const float *trunc_value,
+                           const float *bootstrap, float gamma, int64_t N, int64_t T,
+                           int64_t ld, float *returns, void *stream)
+{
+    if (bad_gamma(gamma)) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma, 1.f,
+                           N, T, ld);
+    p.out0 = returns;
+    const float *in[] = {reward};
+    float *out[] = {returns};
+    return validate_and_launch(p, in, 1, out, 1, rlca::launch_return, stream);
+}
+
+int rlca_td_lambda(const float *reward, const float *value, const uint8_t *terminated,
+                   const uint8_t *truncated, const float *trunc_value,
+                   const float *bootstrap, float gamma, float lambda, int64_t N,
+                   int64_t T, int64_t ld, float *targets, void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambda, N, T, ld);
+    p.value = value;
+    p.out0 = targets;
+    const float *in[] = {reward, value};
+    float *out[] = {targets};
+    return validate_and_launch(p, in, 2, out, 1, rlca::launch_td_lambda, stream);
+}
+
+int rlca_gae(const float *reward, const float *value, const uint8_t *terminated,
+             const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+             float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+             float *advantages, float *returns, void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambda, N, T, ld);
+    p.value = value;
+    p.out0 = advantages;
+    p.out1 = returns;
+    const float *in[] = {reward, value};
+    float *out[] = {advantages, returns};
+    return validate_and_launch(p, in, 2, out, 2, rlca::launch_gae, stream);
+}
+
+int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
+                const uint8_t *terminated, const uint8_t *truncated,
+                const float *trunc_value, const float *bootstrap, float gamma,
+                float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda) || bad_clip(rho_bar) || bad_clip(c_bar) ||
+        bad_clip(pg_rho_bar))
+        return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambda, N, T, ld);
+    p.value = value;
+    p.aux = log_rho;
+    p.rho_bar = rho_bar;
+    p.c_bar = c_bar;
+    p.pg_rho_bar = pg_rho_bar;
+    p.out0 = vs;
+    p.out1 = pg_advantages;
+    const float *in[] = {reward, value, log_rho};
+    float *out[] = {vs, pg_advantages};
+    return validate_and_launch(p, in, 3, out, 2, rlca::launch_vtrace, stream);
+}
+
+int rlca_retrace(const float *reward, const float *q_taken, const float *expected_q,
+                 const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+                 const float *trunc_value, const float *bootstrap_ev, float gamma,
+                 float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                 void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap_ev, gamma,
+                           lambda, N, T, ld);
+    p.value = q_taken;
+    p.aux = expected_q;
+    p.rho = rho;
+    p.out0 = q_ret;
+    const float *in[] = {reward, q_taken, expected_q, rho};
+    float *out[] = {q_ret};
+    return validate_and_launch(p, in, 4, out, 1, rlca::launch_retrace, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,10 @@
+// Kernels of one estimator (instantiated in a translation unit of its own so the
+// library builds in parallel).
+#include "launch.cuh"
+
+namespace rlca {
+cudaError_t launch_retrace(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator<Est::kRetrace>(p, vec, stream);
+}
+}  // namespace rlca

@@ -1,0 +1,217 @@
+// Per-estimator operand builders and epilogues (Method section 2 of "rl-triton:
+// High-Performance Triton GPU Kernels for Reinforcement Learning Credit Assignment":
+// the recurrence coefficients are formed in registers straight from the raw rollout
+// inputs and are never written to memory).
+//
+// Each thread owns ITEMS consecutive steps t0 .. t0+ITEMS-1 of one env row. For every
+// step it forms (alpha_t, beta_t, reset_t) of A_t = alpha_t + beta_t * A_{t+1}:
+//
+//   estimator   alpha_t                                       beta_t          output
+//   return      r_t (+ gamma * sv_t if the episode stops)     gamma           G = A
+//   TD(lambda)  r_t + gamma(1-lambda) V_{t+1}  | r_t+gamma sv  gamma lambda    G = A
+//   GAE         r_t + gamma V(s_{t+1}) - V_t                  gamma lambda    adv = A,
+//                                                                             ret = A + V
+//   V-trace     rho_hat_t (r_t + gamma V(s_{t+1}) - V_t)     gamma c_t       vs = V + A
+//   Retrace     r_t + gamma EQ(s_{t+1}) - Q_t                 gamma c_{t+1}   Q^ret = A + Q
+//
+// where sv_t (successor value, Method section 3) is 0 for a terminated step, the
+// supplied truncation value for a truncated one and the per-env bootstrap at t = T-1;
+// V(s_{t+1}) / EQ(s_{t+1}) is V_{t+1} / E_pi Q_{t+1} inside an episode and sv_t at its
+// last step; reset_t is set exactly at an episode's last step.
+#pragma once
+
+#include "scan_core.cuh"
+
+namespace rlca {
+
+enum class Est : int { kReturn = 0, kTdLambda = 1, kGae = 2, kVtrace = 3, kRetrace = 4 };
+
+// Kernel arguments, passed by value.
+struct Params {
+    const float *reward;
+    const float *value;  // V (TD, GAE, V-trace) or Q(s_t, a_t) (Retrace)
+    const float *aux;    // log importance ratios (V-trace) or E_pi Q(s_t, .) (Retrace)
+    const float *rho;    // importance ratios (Retrace)
+    const uint8_t *term;
+    const uint8_t *trunc;
+    const float *trunc_value;
+    const float *boot;
+    float *out0;
+    float *out1;  // nullable
+    int64_t N;
+    int64_t ld;
+    int T;
+    float gamma;
+    float lambda;
+    float gamma_lambda;        // gamma * lambda, rounded to fp32
+    float gamma_one_m_lambda;  // gamma * (1 - lambda), rounded to fp32
+    float rho_bar;
+    float c_bar;
+    float pg_rho_bar;
+    // Geometry of the launch (see kernels.cuh).
+    int rows_per_tile;
+    int chunks_per_row;
+    int segs;
+};
+
+template <Est E>
+struct EstTraits {
+    static constexpr bool kValue = E != Est::kReturn;
+    static constexpr bool kAux = E == Est::kVtrace || E == Est::kRetrace;
+    static constexpr bool kRho = E == Est::kRetrace;
+    static constexpr bool kNextValue =
+        E == Est::kTdLambda || E == Est::kGae || E == Est::kVtrace;
+    static constexpr bool kNextAux = E == Est::kRetrace;
+    static constexpr bool kNextRho = E == Est::kRetrace;
+    static constexpr bool kTwoOutputs = E == Est::kGae || E == Est::kVtrace;
+};
+
+// Raw inputs of one thread's ITEMS steps, plus the successor (step t0+ITEMS) of the
+// arrays whose next step an estimator reads.
+template <int ITEMS>
+struct Chunk {
+    float r[ITEMS];
+    float v[ITEMS];
+    float x[ITEMS];
+    float y[ITEMS];
+    float sv[ITEMS];  // successor value at steps where the episode stops
+    float v_next, x_next, y_next;
+    unsigned stop;   // bit j: the recursion stops at step j (boundary or padding)
+    unsigned valid;  // bit j: step t0+j exists in this row
+};
+
+// Successor of item ITEMS-1: the next lane's first item, or (lane 31) a direct load.
+// Every lane of the warp must call this (it shuffles).
+__device__ __forceinline__ float next_item(float first_item, const float *__restrict__ row,
+                                           int t_next, bool need, int lane)
+{
+    float s = __shfl_down_sync(kFullMask, first_item, 1);
+    if (lane == 31) s = need ? __ldg(row + t_next) : 0.f;
+    return need ? s : 0.f;
+}
+
+template <Est E, int ITEMS, bool VEC, bool TRUNC>
+__device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0, bool active,
+                                           int lane, Chunk<ITEMS> &c)
+{
+    using Tr = EstTraits<E>;
+    const int T = p.T;
+    const int Te = active ? T : 0;  // an inactive thread sees an empty row
+    const int64_t off = active ? row * p.ld : 0;
+
+    load_items<ITEMS, VEC>(p.reward + off, t0, Te, c.r);
+    if (Tr::kValue) load_items<ITEMS, VEC>(p.value + off, t0, Te, c.v);
+    if (Tr::kAux) load_items<ITEMS, VEC>(p.aux + off, t0, Te, c.x);
+    if (Tr::kRho) load_items<ITEMS, VEC>(p.rho + off, t0, Te, c.y);
+    const unsigned term = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
+    const unsigned trunc = TRUNC ? load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te) : 0u;
+
+    unsigned valid = 0;
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) valid |= (t0 + j < Te ? 1u : 0u) << j;
+    const int last = T - 1 - t0;
+    const unsigned window_end = (last >= 0 && last < ITEMS) ? (1u << last) : 0u;
+    const unsigned all = (ITEMS == 32) ? 0xffffffffu : ((1u << ITEMS) - 1u);
+    c.valid = valid;
+    c.stop = (term | trunc | window_end | ~valid) & all;
+
+    const bool need = active && (t0 + ITEMS < T);
+    if (Tr::kNextValue) c.v_next = next_item(c.v[0], p.value + off, t0 + ITEMS, need, lane);
+    if (Tr::kNextAux) c.x_next = next_item(c.x[0], p.aux + off, t0 + ITEMS, need, lane);
+    if (Tr::kNextRho) c.y_next = next_item(c.y[0], p.rho + off, t0 + ITEMS, need, lane);
+
+    // Successor values where an episode stops (Method section 3): termination 0, then
+    // truncation (value read only where truncated), then the window-end bootstrap.
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        float s = 0.f;
+        const unsigned bit = 1u << j;
+        if ((valid & bit) && !(term & bit)) {
+            if (trunc & bit)
+                s = __ldg(p.trunc_value + off + t0 + j);
+            else if (window_end & bit)
+                s = p.boot ? __ldg(p.boot + row) : 0.f;
+        }
+        c.sv[j] = s;
+    }
+}
+
+template <int ITEMS>
+__device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next, int j)
+{
+    return (j + 1 < ITEMS) ? a[j + 1] : next;
+}
+
+// Forms (alpha, beta, reset) of every item. V-trace keeps rho_t in c.x for the epilogue.
+template <Est E, int ITEMS>
+__device__ __forceinline__ void build(const Params &p, Chunk<ITEMS> &c, Affine (&e)[ITEMS])
+{
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        const bool stop = (c.stop >> j) & 1u;
+        const float r = c.r[j];
+        float a, b;
+        if (E == Est::kReturn) {
+            a = stop ? fmaf(p.gamma, c.sv[j], r) : r;
+            b = p.gamma;
+        } else if (E == Est::kTdLambda) {
+            a = stop ? fmaf(p.gamma, c.sv[j], r)
+                     : fmaf(p.gamma_one_m_lambda, at_or_next(c.v, c.v_next, j), r);
+            b = p.gamma_lambda;
+        } else if (E == Est::kGae) {
+            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
+            a = fmaf(p.gamma, nxt, r) - c.v[j];
+            b = p.gamma_lambda;
+        } else if (E == Est::kVtrace) {
+            const float rho = expf(c.x[j]);
+            c.x[j] = rho;
+            const float rho_hat = rho < p.rho_bar ? rho : p.rho_bar;
+            const float cc = p.lambda * (rho < p.c_bar ? rho : p.c_bar);
+            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
+            a = rho_hat * (fmaf(p.gamma, nxt, r) - c.v[j]);
+            b = p.gamma * cc;
+        } else {  // Retrace
+            const float rho1 = at_or_next(c.y, c.y_next, j);
+            const float c1 = p.lambda * (rho1 < 1.f ? rho1 : 1.f);
+            const float nxt = stop ? c.sv[j] : at_or_next(c.x, c.x_next, j);
+            a = fmaf(p.gamma, nxt, r) - c.v[j];
+            b = p.gamma * c1;
+        }
+        e[j] = Affine{a, b, stop ? 1 : 0};
+    }
+}
+
+// Outputs of every item from A_t (A[j]) and A at the step after the chunk (a_after).
+template <Est E, int ITEMS, bool VEC>
+__device__ __forceinline__ void epilogue(const Params &p, const Chunk<ITEMS> &c,
+                                         const float (&A)[ITEMS], float a_after, int64_t row,
+                                         int t0)
+{
+    if (!c.valid) return;
+    const int64_t off = row * p.ld;
+    float o0[ITEMS];
+    float o1[ITEMS];
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        if (E == Est::kReturn || E == Est::kTdLambda) {
+            o0[j] = A[j];
+        } else if (E == Est::kGae) {
+            o0[j] = A[j];
+            o1[j] = A[j] + c.v[j];
+        } else if (E == Est::kVtrace) {
+            const bool stop = (c.stop >> j) & 1u;
+            const float rho = c.x[j];
+            const float a_next = (j + 1 < ITEMS) ? A[j + 1] : a_after;
+            const float q = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j) + a_next;
+            const float rho_pg = rho < p.pg_rho_bar ? rho : p.pg_rho_bar;
+            o0[j] = c.v[j] + A[j];
+            o1[j] = rho_pg * (fmaf(p.gamma, q, c.r[j]) - c.v[j]);
+        } else {
+            o0[j] = A[j] + c.v[j];
+        }
+    }
+    store_items<ITEMS, VEC>(p.out0 + off, t0, c.valid, o0);
+    if (EstTraits<E>::kTwoOutputs && p.out1) store_items<ITEMS, VEC>(p.out1 + off, t0, c.valid, o1);
+}
+
+}  // namespace rlca

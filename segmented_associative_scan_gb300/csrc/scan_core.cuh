@@ -1,0 +1,132 @@
+// Segmented reverse affine scan: the on-chip core shared by every estimator kernel.
+//
+// Method section 1 of "rl-triton: High-Performance Triton GPU Kernels for Reinforcement
+// Learning Credit Assignment": every estimator is A_t = alpha_t + beta_t * A_{t+1}, an
+// associative scan over pairs (alpha, beta) with
+//   (aB, bB) (+) (aA, bA) = (aB + bB * aA, bA * bB),   B the earlier step, A the later.
+// Method section 3 (episode boundaries) enters as an explicit reset flag: a step whose
+// episode ends there takes nothing from t+1. The flag is a select, not a multiply by 0,
+// so a NaN or Inf in a later episode never reaches an earlier one.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rlca {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// The map x -> a + b * x, or the constant a when f is set (an episode ends inside).
+struct Affine {
+    float a;
+    float b;
+    int f;
+};
+
+__device__ __forceinline__ Affine affine_identity() { return Affine{0.f, 1.f, 0}; }
+
+__device__ __forceinline__ float affine_apply(const Affine &e, float x)
+{
+    return e.f ? e.a : fmaf(e.b, x, e.a);
+}
+
+// The pages' operator: `early` applied after `late` (early covers smaller t).
+__device__ __forceinline__ Affine affine_compose(const Affine &early, const Affine &late)
+{
+    Affine r;
+    r.a = early.f ? early.a : fmaf(early.b, late.a, early.a);
+    r.b = early.f ? early.b : early.b * late.b;
+    r.f = early.f | late.f;
+    return r;
+}
+
+__device__ __forceinline__ Affine shfl_down(const Affine &x, int d)
+{
+    Affine y;
+    y.a = __shfl_down_sync(kFullMask, x.a, d);
+    y.b = __shfl_down_sync(kFullMask, x.b, d);
+    y.f = __shfl_down_sync(kFullMask, x.f, d);
+    return y;
+}
+
+// Inclusive suffix scan across a warp: lane i gets x_i (+) x_{i+1} (+) ... (+) x_31.
+__device__ __forceinline__ Affine warp_suffix_scan(Affine x, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        Affine y = shfl_down(x, d);
+        if (lane + d < 32) x = affine_compose(x, y);
+    }
+    return x;
+}
+
+// ---------------------------------------------------------------- memory access
+
+// Streaming loads/stores: every input is read once and every output written once.
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ float ld_stream(const float *p) { return __ldcs(p); }
+__device__ __forceinline__ uint32_t ld_stream(const uint32_t *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(float *p, float v) { __stcs(p, v); }
+
+// ITEMS consecutive floats of one row starting at column t0; columns >= T read as 0.
+template <int ITEMS, bool VEC>
+__device__ __forceinline__ void load_items(const float *__restrict__ row, int t0, int T,
+                                           float (&x)[ITEMS])
+{
+    if (VEC && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k) {
+            float4 q = ld_stream(reinterpret_cast<const float4 *>(row + t0) + k);
+            x[4 * k + 0] = q.x;
+            x[4 * k + 1] = q.y;
+            x[4 * k + 2] = q.z;
+            x[4 * k + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) x[j] = (t0 + j < T) ? ld_stream(row + t0 + j) : 0.f;
+    }
+}
+
+// Bit j set when flag byte (t0 + j) is nonzero; columns >= T read as clear.
+template <int ITEMS, bool VEC>
+__device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ row, int t0,
+                                                   int T)
+{
+    unsigned bits = 0;
+    if (VEC && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k) {
+            uint32_t w = ld_stream(reinterpret_cast<const uint32_t *>(row + t0) + k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                bits |= (((w >> (8 * i)) & 0xffu) != 0u ? 1u : 0u) << (4 * k + i);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j)
+            if (t0 + j < T && row[t0 + j] != 0) bits |= 1u << j;
+    }
+    return bits;
+}
+
+// Store the valid items (bit j of `valid`) of ITEMS consecutive floats.
+template <int ITEMS, bool VEC>
+__device__ __forceinline__ void store_items(float *__restrict__ row, int t0, unsigned valid,
+                                            const float (&x)[ITEMS])
+{
+    constexpr unsigned kAll = (ITEMS == 32) ? 0xffffffffu : ((1u << ITEMS) - 1u);
+    if (VEC && valid == kAll) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k)
+            st_stream(reinterpret_cast<float4 *>(row + t0) + k,
+                      make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j)
+            if (valid & (1u << j)) st_stream(row + t0 + j, x[j]);
+    }
+}
+
+}  // namespace rlca

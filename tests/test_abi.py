@@ -1,0 +1,109 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/rlca.h declares,
+and rejects bad arguments on the host with the documented status codes before any
+CUDA call (these tests run without a GPU; the pointers are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import segmented_associative_scan_gb300 as rlca
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlca.h")
+
+OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rlca.build()
+    return rlca.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlca_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "rlca_gae" in names and "rlca_retrace" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in rlca.h but not exported"
+        assert name in rlca.SIGNATURES, f"{name} has no Python binding"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.rlca_version() >= 100
+    for code in (OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT):
+        assert lib.rlca_status_string(code)
+    assert b"unknown" in lib.rlca_status_string(12345)
+
+
+# Fake, never-dereferenced device addresses, 256 bytes apart per row block.
+def fake(i, N=4, T=64):
+    return 0x10000000 + i * 0x100000
+
+
+def gae_args(**kw):
+    a = dict(reward=fake(1), value=fake(2), term=fake(3), trunc=None, tv=None, boot=None,
+             gamma=0.99, lam=0.95, N=4, T=64, ld=64, adv=fake(4), ret=fake(5), stream=None)
+    a.update(kw)
+    return (a["reward"], a["value"], a["term"], a["trunc"], a["tv"], a["boot"], a["gamma"],
+            a["lam"], a["N"], a["T"], a["ld"], a["adv"], a["ret"], a["stream"])
+
+
+def test_null_pointers(lib):
+    assert lib.rlca_gae(*gae_args(reward=None)) == NULL
+    assert lib.rlca_gae(*gae_args(value=None)) == NULL
+    assert lib.rlca_gae(*gae_args(term=None)) == NULL
+    assert lib.rlca_gae(*gae_args(adv=None)) == NULL
+    assert lib.rlca_gae(*gae_args(trunc=fake(6))) == NULL  # truncated without values
+    assert lib.rlca_discounted_return(fake(1), fake(2), None, None, None, 0.9, 4, 64, 64,
+                                      None, None) == NULL
+    assert lib.rlca_retrace(fake(1), fake(2), None, fake(3), fake(4), None, None, None,
+                            0.99, 0.95, 4, 64, 64, fake(5), None) == NULL
+
+
+def test_shapes(lib):
+    assert lib.rlca_gae(*gae_args(N=-1)) == SHAPE
+    assert lib.rlca_gae(*gae_args(T=-1)) == SHAPE
+    assert lib.rlca_gae(*gae_args(ld=63)) == SHAPE
+    assert lib.rlca_gae(*gae_args(T=(1 << 30) + 1, ld=(1 << 30) + 1)) == SHAPE
+    assert lib.rlca_gae(*gae_args(N=1 << 40, T=1 << 20, ld=1 << 22)) == SHAPE
+
+
+def test_empty_problems_are_no_ops(lib):
+    # N == 0 or T == 0: valid, nothing enqueued, pointers may be NULL.
+    assert lib.rlca_gae(*gae_args(N=0, reward=None, value=None, term=None, adv=None)) == OK
+    assert lib.rlca_gae(*gae_args(T=0, ld=0, reward=None, adv=None)) == OK
+    assert lib.rlca_vtrace(None, None, None, None, None, None, None, 0.99, 1.0, 1.0, 1.0,
+                           1.0, 0, 16, 16, None, None, None) == OK
+
+
+def test_parameters(lib):
+    for g in (-0.1, float("nan"), float("inf")):
+        assert lib.rlca_gae(*gae_args(gamma=g)) == PARAM
+    for lam in (-0.01, 1.01, float("nan")):
+        assert lib.rlca_gae(*gae_args(lam=lam)) == PARAM
+    assert lib.rlca_td_lambda(fake(1), fake(2), fake(3), None, None, None, 0.9, 2.0, 4, 64,
+                              64, fake(4), None) == PARAM
+    v = lambda rb, cb, pb: lib.rlca_vtrace(fake(1), fake(2), fake(3), fake(4), None, None,
+                                           None, 0.99, 1.0, rb, cb, pb, 4, 64, 64, fake(5),
+                                           fake(6), None)
+    assert v(0.0, 1.0, 1.0) == PARAM
+    assert v(1.0, float("nan"), 1.0) == PARAM
+    assert v(1.0, 1.0, -1.0) == PARAM
+
+
+def test_aliasing(lib):
+    N, T = 4, 64
+    row_bytes = T * 4
+    assert lib.rlca_gae(*gae_args(adv=fake(1))) == ALIAS  # output == reward
+    assert lib.rlca_gae(*gae_args(adv=fake(1) + 8)) == ALIAS  # inside reward
+    assert lib.rlca_gae(*gae_args(ret=fake(4))) == ALIAS  # two outputs equal
+    assert lib.rlca_gae(*gae_args(adv=fake(3) - 16)) == ALIAS  # runs into the flags
+    assert lib.rlca_discounted_return(fake(1), fake(2), None, None, fake(3), 0.9, N, T, T,
+                                      fake(3) - 8, None) == ALIAS  # overlaps bootstrap
