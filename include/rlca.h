@@ -31,8 +31,9 @@
  *             current device; all work is enqueued on it, asynchronously. Pointers must
  *             belong to the current device.
  *   Ownership The caller owns every buffer. The library never allocates or frees
- *             memory, never synchronises, and never changes the current device. Inputs
- *             are read only. Outputs must not overlap any input or each other.
+ *             memory, never changes the current device and never synchronises (except
+ *             rlca_workspace_check, which says so). Inputs are read only. Outputs must
+ *             not overlap any input or each other.
  *   Errors    0 = RLCA_OK. A negative code means nothing was enqueued, except
  *             RLCA_ERR_LAUNCH (the launch itself failed; cudaGetLastError is cleared).
  *             N == 0 or T == 0 is a valid empty problem: RLCA_OK, nothing enqueued.
@@ -140,6 +141,82 @@ int rlca_retrace(const float *reward, const float *q_taken, const float *expecte
                  const float *trunc_value, const float *bootstrap_ev, float gamma,
                  float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
                  void *stream);
+
+/*
+ * Long sequences: tiles scanned in parallel with decoupled look-back.
+ *
+ * The kernels scan tiles of 1024 steps. When T > 1024 a row spans several tiles. The
+ * entry points above walk the tiles of a row one after another inside one CTA, carrying
+ * A between them in registers. The _ex variants below take a caller-owned device
+ * workspace and instead launch one CTA per tile for all tiles of all rows at once; a
+ * tile finds its carry-in from the later tiles of its row by decoupled look-back
+ * (Merrill & Garland 2016), which helps when N alone is too small to fill the GPU.
+ * This realises Method section 1's O(log T)-depth scan across CTAs with one HBM read
+ * and one write (Method section 2).
+ *
+ * Workspace: rlca_workspace_bytes(N, T) bytes of device memory, 256-byte aligned,
+ * zero-filled once before its first use (e.g. cudaMemsetAsync to 0). Each call leaves
+ * it ready for the next, so it is zeroed only once. Calls that share a workspace must
+ * not run concurrently on the GPU (use one stream, or order the streams). The workspace
+ * may overlap no input or output (RLCA_ERR_ALIAS).
+ * When rlca_workspace_bytes returns 0 (T <= 1024: rows never span tiles) an _ex call
+ * ignores the workspace and behaves exactly as the plain call.
+ *
+ * Bounded waits: a tile polls the state of a later tile at most about a second; if it
+ * gives up it marks its outputs NaN and records RLCA_ERR_TIMEOUT in the workspace. No
+ * wait can hang the GPU. rlca_workspace_check reports and clears that record.
+ */
+
+/* Bytes of workspace an _ex call needs for [N, T]: 256 + 32 * N * ceil(T / 1024) when
+ * T > 1024, else 0. Returns 0 for invalid shapes. */
+size_t rlca_workspace_bytes(int64_t N, int64_t T);
+
+/* Synchronises `stream`, then returns RLCA_OK, or RLCA_ERR_TIMEOUT if a look-back wait
+ * on this workspace gave up since the last check (the record is then cleared), or
+ * RLCA_ERR_LAUNCH if a CUDA call failed. This is the only entry point that blocks. */
+int rlca_workspace_check(void *workspace, void *stream);
+
+int rlca_discounted_return_ex(const float *reward, const uint8_t *terminated,
+                              const uint8_t *truncated, const float *trunc_value,
+                              const float *bootstrap, float gamma, int64_t N, int64_t T,
+                              int64_t ld, float *returns, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+int rlca_td_lambda_ex(const float *reward, const float *value, const uint8_t *terminated,
+                      const uint8_t *truncated, const float *trunc_value,
+                      const float *bootstrap, float gamma, float lambda, int64_t N,
+                      int64_t T, int64_t ld, float *targets, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+int rlca_gae_ex(const float *reward, const float *value, const uint8_t *terminated,
+                const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+                float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+                float *advantages, float *returns, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+int rlca_vtrace_ex(const float *reward, const float *value, const float *log_rho,
+                   const uint8_t *terminated, const uint8_t *truncated,
+                   const float *trunc_value, const float *bootstrap, float gamma,
+                   float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                   int64_t T, int64_t ld, float *vs, float *pg_advantages, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+int rlca_retrace_ex(const float *reward, const float *q_taken, const float *expected_q,
+                    const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+                    const float *trunc_value, const float *bootstrap_ev, float gamma,
+                    float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Testing only: runs the look-back discounted return (gamma 0.99, no truncation, no
+ * bootstrap, ld = T) with every tile withholding its state, so each waiting tile gives
+ * up after `spin_limit` empty polls. Afterwards rlca_workspace_check returns
+ * RLCA_ERR_TIMEOUT and the workspace is ready for normal calls again. Needs T > 1024
+ * and spin_limit > 0 (else RLCA_ERR_WORKSPACE).
+ */
+int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, int64_t N,
+                                int64_t T, float *returns, void *workspace,
+                                size_t workspace_bytes, int spin_limit, void *stream);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,16 @@ SIGNATURES = {
                      _P, _P], ctypes.c_int),
     "rlca_retrace": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P],
                      ctypes.c_int),
+    "rlca_workspace_bytes": ([_I64, _I64], ctypes.c_size_t),
+    "rlca_workspace_check": ([_P, _P], ctypes.c_int),
+    "rlca_testing_lookback_stall": ([_P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, ctypes.c_int,
+                                     _P], ctypes.c_int),
 }
+# The _ex variants take (workspace, workspace_bytes) before the stream.
+for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
+              "rlca_retrace"):
+    _args, _res = SIGNATURES[_name]
+    SIGNATURES[_name + "_ex"] = (_args[:-1] + [_P, ctypes.c_size_t, _P], _res)
 
 _lib = None
 
@@ -130,34 +139,65 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def workspace_bytes(N: int, T: int) -> int:
+    """Bytes of look-back workspace an [N, T] call needs (0: none needed)."""
+    return int(lib().rlca_workspace_bytes(N, T))
+
+
+def make_workspace(N: int, T: int, device="cuda") -> torch.Tensor | None:
+    """A zero-filled workspace tensor for the _ex (look-back) path, or None when
+    T fits one tile. PyTorch allocates it; the library never allocates."""
+    n = workspace_bytes(N, T)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+
+
+def workspace_check(workspace: torch.Tensor) -> int:
+    """Synchronise the current stream and return the workspace's status
+    (0, or -7 after a look-back wait gave up; the record is then cleared)."""
+    return int(lib().rlca_workspace_check(workspace.data_ptr(), _stream(workspace.device)))
+
+
+def _call(name, args, workspace, stream):
+    """Call the plain entry point, or its _ex variant when a workspace is given."""
+    if workspace is None:
+        return getattr(lib(), name)(*args, stream)
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    return getattr(lib(), name + "_ex")(*args, workspace.data_ptr(),
+                                        workspace.numel(), stream)
+
+
 def rlca_discounted_return(reward, terminated, truncated=None, trunc_value=None,
-                           bootstrap=None, gamma=0.99, returns=None):
+                           bootstrap=None, gamma=0.99, returns=None, workspace=None):
     g = _Rows(reward)
     args = (g.ptr(reward, "reward", _F32), g.ptr(terminated, "terminated", _FLAG),
             g.ptr(truncated, "truncated", _FLAG, True),
             g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     returns = g.out(returns, "returns")
-    _check("rlca_discounted_return", lib().rlca_discounted_return(
-        *args, gamma, g.N, g.T, g.ld, returns.data_ptr() or None, _stream(g.device)))
+    _check("rlca_discounted_return", _call(
+        "rlca_discounted_return", (*args, gamma, g.N, g.T, g.ld, returns.data_ptr() or None),
+        workspace, _stream(g.device)))
     return returns
 
 
 def rlca_td_lambda(reward, value, terminated, truncated=None, trunc_value=None,
-                   bootstrap=None, gamma=0.99, lam=0.95, targets=None):
+                   bootstrap=None, gamma=0.99, lam=0.95, targets=None, workspace=None):
     g = _Rows(reward)
     args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
             g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
             g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     targets = g.out(targets, "targets")
-    _check("rlca_td_lambda", lib().rlca_td_lambda(
-        *args, gamma, lam, g.N, g.T, g.ld, targets.data_ptr() or None, _stream(g.device)))
+    _check("rlca_td_lambda", _call(
+        "rlca_td_lambda", (*args, gamma, lam, g.N, g.T, g.ld, targets.data_ptr() or None),
+        workspace, _stream(g.device)))
     return targets
 
 
 def rlca_gae(reward, value, terminated, truncated=None, trunc_value=None, bootstrap=None,
-             gamma=0.99, lam=0.95, advantages=None, returns=None, want_returns=True):
+             gamma=0.99, lam=0.95, advantages=None, returns=None, want_returns=True,
+             workspace=None):
     g = _Rows(reward)
     args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
             g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
@@ -165,15 +205,16 @@ def rlca_gae(reward, value, terminated, truncated=None, trunc_value=None, bootst
             g.vec_ptr(bootstrap, "bootstrap"))
     advantages = g.out(advantages, "advantages")
     returns = g.out(returns, "returns") if (want_returns or returns is not None) else None
-    _check("rlca_gae", lib().rlca_gae(
-        *args, gamma, lam, g.N, g.T, g.ld, advantages.data_ptr() or None,
-        returns.data_ptr() or None if returns is not None else None, _stream(g.device)))
+    _check("rlca_gae", _call(
+        "rlca_gae", (*args, gamma, lam, g.N, g.T, g.ld, advantages.data_ptr() or None,
+                     returns.data_ptr() or None if returns is not None else None),
+        workspace, _stream(g.device)))
     return advantages, returns
 
 
 def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=None,
                 bootstrap=None, gamma=0.99, lam=1.0, rho_bar=1.0, c_bar=1.0,
-                pg_rho_bar=None, vs=None, pg_advantages=None, want_pg=True):
+                pg_rho_bar=None, vs=None, pg_advantages=None, want_pg=True, workspace=None):
     g = _Rows(reward)
     args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
             g.ptr(log_rho, "log_rho", _F32), g.ptr(terminated, "terminated", _FLAG),
@@ -185,15 +226,17 @@ def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=
         else None
     if pg_rho_bar is None:
         pg_rho_bar = rho_bar
-    _check("rlca_vtrace", lib().rlca_vtrace(
-        *args, gamma, lam, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld,
-        vs.data_ptr() or None, pg.data_ptr() or None if pg is not None else None,
-        _stream(g.device)))
+    _check("rlca_vtrace", _call(
+        "rlca_vtrace", (*args, gamma, lam, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld,
+                        vs.data_ptr() or None,
+                        pg.data_ptr() or None if pg is not None else None),
+        workspace, _stream(g.device)))
     return vs, pg
 
 
 def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
-                 trunc_value=None, bootstrap_ev=None, gamma=0.99, lam=0.95, q_ret=None):
+                 trunc_value=None, bootstrap_ev=None, gamma=0.99, lam=0.95, q_ret=None,
+                 workspace=None):
     g = _Rows(reward)
     args = (g.ptr(reward, "reward", _F32), g.ptr(q_taken, "q_taken", _F32),
             g.ptr(expected_q, "expected_q", _F32), g.ptr(rho, "rho", _F32),
@@ -201,8 +244,9 @@ def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
             g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
             g.vec_ptr(bootstrap_ev, "bootstrap_ev"))
     q_ret = g.out(q_ret, "q_ret")
-    _check("rlca_retrace", lib().rlca_retrace(
-        *args, gamma, lam, g.N, g.T, g.ld, q_ret.data_ptr() or None, _stream(g.device)))
+    _check("rlca_retrace", _call(
+        "rlca_retrace", (*args, gamma, lam, g.N, g.T, g.ld, q_ret.data_ptr() or None),
+        workspace, _stream(g.device)))
     return q_ret
 
 

@@ -1,6 +1,6 @@
 // C ABI of librlca (declared in include/rlca.h): argument validation, then one fused
-// kernel launch on the caller's stream. No allocation, no synchronisation, no change
-// of the current device.
+// kernel launch on the caller's stream. No allocation, no synchronisation (except in
+// rlca_workspace_check, which says so), no change of the current device.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -41,11 +41,16 @@ bool bad_gamma(float g) { return !std::isfinite(g) || g < 0.f; }
 bool bad_lambda(float l) { return !(l >= 0.f && l <= 1.f); }
 bool bad_clip(float c) { return std::isnan(c) || !(c > 0.f); }
 
-// Common validation of the optional/required inputs and the outputs, then launch.
-// `f32_in` are the required float inputs read with vector loads, `outs` the outputs.
+struct Workspace {
+    void *ptr;
+    size_t bytes;
+};
+
+// Common validation of inputs, outputs and workspace, then launch.
+// `f32_in` are the required float inputs, `outs` the outputs (outs[0] required).
 template <typename LaunchFn>
 int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *const *outs,
-                        int n_out, LaunchFn launch, void *stream)
+                        int n_out, Workspace ws, LaunchFn launch, void *stream)
 {
     // An empty problem is valid whatever the pointers (an empty tensor may have none).
     bool empty = false;
@@ -74,6 +79,21 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
             if (overlaps(ro, in_ranges[i])) return RLCA_ERR_ALIAS;
         for (int q = o + 1; q < n_out; ++q)
             if (outs[q] && overlaps(ro, span(outs[q], p.N, p.T, p.ld, 4))) return RLCA_ERR_ALIAS;
+    }
+
+    // The workspace is used only when a row spans several tiles.
+    p.ws = nullptr;
+    const size_t need = rlca::workspace_bytes(p.N, p.T);
+    if (ws.ptr && need > 0 && rlca::lookback_tiles(p.N, p.T) <= INT32_MAX) {
+        if (ws.bytes < need || !aligned(ws.ptr, 256)) return RLCA_ERR_WORKSPACE;
+        const Range rw{reinterpret_cast<uintptr_t>(ws.ptr),
+                       reinterpret_cast<uintptr_t>(ws.ptr) + need};
+        for (int i = 0; i < k; ++i)
+            if (overlaps(rw, in_ranges[i])) return RLCA_ERR_ALIAS;
+        for (int o = 0; o < n_out; ++o)
+            if (outs[o] && overlaps(rw, span(outs[o], p.N, p.T, p.ld, 4))) return RLCA_ERR_ALIAS;
+        p.ws = ws.ptr;
+        if (p.spin_limit <= 0) p.spin_limit = rlca::kDefaultSpinLimit;
     }
 
     // 128-bit loads/stores need 16-byte aligned rows: ld % 4 == 0 and aligned bases.
@@ -107,45 +127,26 @@ Params base_params(const float *reward, const uint8_t *term, const uint8_t *trun
     return p;
 }
 
-}  // namespace
-
-extern "C" {
-
-int rlca_version(void) { return 100; }
-
-const char *rlca_status_string(int status)
-{
-    switch (status) {
-    case RLCA_OK: return "ok";
-    case RLCA_ERR_NULL: return "a required pointer is NULL";
-    case RLCA_ERR_SHAPE: return "invalid shape (N < 0, T < 0, ld < T, T too large, or N*ld overflows)";
-    case RLCA_ERR_PARAM: return "invalid parameter (gamma < 0 or not finite, lambda outside [0,1], or a clip <= 0)";
-    case RLCA_ERR_ALIAS: return "an output overlaps an input or another output";
-    case RLCA_ERR_WORKSPACE: return "workspace too small or misaligned";
-    case RLCA_ERR_LAUNCH: return "CUDA kernel launch failed";
-    case RLCA_ERR_TIMEOUT: return "a bounded cross-block wait timed out";
-    default: return "unknown status";
-    }
-}
-
-int rlca_discounted_return(const float *reward, const uint8_t *terminated,
-                           const uint8_t *truncated, const float *trunc_value,
-                           const float *bootstrap, float gamma, int64_t N, int64_t T,
-                           int64_t ld, float *returns, void *stream)
+int discounted_return(const float *reward, const uint8_t *terminated, const uint8_t *truncated,
+                      const float *trunc_value, const float *bootstrap, float gamma, int64_t N,
+                      int64_t T, int64_t ld, float *returns, Workspace ws, void *stream,
+                      int spin_limit = 0, int stall = 0)
 {
     if (bad_gamma(gamma)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma, 1.f,
                            N, T, ld);
     p.out0 = returns;
+    p.spin_limit = spin_limit;
+    p.stall = stall;
     const float *in[] = {reward};
     float *out[] = {returns};
-    return validate_and_launch(p, in, 1, out, 1, rlca::launch_return, stream);
+    return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return, stream);
 }
 
-int rlca_td_lambda(const float *reward, const float *value, const uint8_t *terminated,
-                   const uint8_t *truncated, const float *trunc_value,
-                   const float *bootstrap, float gamma, float lambda, int64_t N,
-                   int64_t T, int64_t ld, float *targets, void *stream)
+int td_lambda(const float *reward, const float *value, const uint8_t *terminated,
+              const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+              float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
+              Workspace ws, void *stream)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -154,13 +155,13 @@ int rlca_td_lambda(const float *reward, const float *value, const uint8_t *termi
     p.out0 = targets;
     const float *in[] = {reward, value};
     float *out[] = {targets};
-    return validate_and_launch(p, in, 2, out, 1, rlca::launch_td_lambda, stream);
+    return validate_and_launch(p, in, 2, out, 1, ws, rlca::launch_td_lambda, stream);
 }
 
-int rlca_gae(const float *reward, const float *value, const uint8_t *terminated,
-             const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
-             float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
-             float *advantages, float *returns, void *stream)
+int gae(const float *reward, const float *value, const uint8_t *terminated,
+        const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+        float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *advantages,
+        float *returns, Workspace ws, void *stream)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -170,14 +171,14 @@ int rlca_gae(const float *reward, const float *value, const uint8_t *terminated,
     p.out1 = returns;
     const float *in[] = {reward, value};
     float *out[] = {advantages, returns};
-    return validate_and_launch(p, in, 2, out, 2, rlca::launch_gae, stream);
+    return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae, stream);
 }
 
-int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
-                const uint8_t *terminated, const uint8_t *truncated,
-                const float *trunc_value, const float *bootstrap, float gamma,
-                float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
-                int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream)
+int vtrace(const float *reward, const float *value, const float *log_rho,
+           const uint8_t *terminated, const uint8_t *truncated, const float *trunc_value,
+           const float *bootstrap, float gamma, float lambda, float rho_bar, float c_bar,
+           float pg_rho_bar, int64_t N, int64_t T, int64_t ld, float *vs,
+           float *pg_advantages, Workspace ws, void *stream)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda) || bad_clip(rho_bar) || bad_clip(c_bar) ||
         bad_clip(pg_rho_bar))
@@ -193,14 +194,13 @@ int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
     p.out1 = pg_advantages;
     const float *in[] = {reward, value, log_rho};
     float *out[] = {vs, pg_advantages};
-    return validate_and_launch(p, in, 3, out, 2, rlca::launch_vtrace, stream);
+    return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace, stream);
 }
 
-int rlca_retrace(const float *reward, const float *q_taken, const float *expected_q,
-                 const float *rho, const uint8_t *terminated, const uint8_t *truncated,
-                 const float *trunc_value, const float *bootstrap_ev, float gamma,
-                 float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
-                 void *stream)
+int retrace(const float *reward, const float *q_taken, const float *expected_q,
+            const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+            const float *trunc_value, const float *bootstrap_ev, float gamma, float lambda,
+            int64_t N, int64_t T, int64_t ld, float *q_ret, Workspace ws, void *stream)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap_ev, gamma,
@@ -211,7 +211,166 @@ int rlca_retrace(const float *reward, const float *q_taken, const float *expecte
     p.out0 = q_ret;
     const float *in[] = {reward, q_taken, expected_q, rho};
     float *out[] = {q_ret};
-    return validate_and_launch(p, in, 4, out, 1, rlca::launch_retrace, stream);
+    return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
+}
+
+constexpr Workspace kNoWorkspace{nullptr, 0};
+
+}  // namespace
+
+extern "C" {
+
+int rlca_version(void) { return 200; }
+
+const char *rlca_status_string(int status)
+{
+    switch (status) {
+    case RLCA_OK: return "ok";
+    case RLCA_ERR_NULL: return "a required pointer is NULL";
+    case RLCA_ERR_SHAPE: return "invalid shape (N < 0, T < 0, ld < T, T too large, or N*ld overflows)";
+    case RLCA_ERR_PARAM: return "invalid parameter (gamma < 0 or not finite, lambda outside [0,1], or a clip <= 0)";
+    case RLCA_ERR_ALIAS: return "an output or the workspace overlaps an input or another output";
+    case RLCA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case RLCA_ERR_LAUNCH: return "CUDA call failed";
+    case RLCA_ERR_TIMEOUT: return "a bounded cross-block wait timed out";
+    default: return "unknown status";
+    }
+}
+
+size_t rlca_workspace_bytes(int64_t N, int64_t T)
+{
+    if (N <= 0 || T <= 0 || T > RLCA_MAX_T) return 0;
+    return rlca::workspace_bytes(N, T);
+}
+
+int rlca_workspace_check(void *workspace, void *stream)
+{
+    if (!workspace) return RLCA_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int *err_dev = &static_cast<rlca::LookbackHeader *>(workspace)->error;
+    int err = 0;
+    if (cudaMemcpyAsync(&err, err_dev, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return RLCA_ERR_LAUNCH;
+    if (err != 0) {
+        if (cudaMemsetAsync(err_dev, 0, sizeof(int), s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return RLCA_ERR_LAUNCH;
+        return RLCA_ERR_TIMEOUT;
+    }
+    return RLCA_OK;
+}
+
+int rlca_discounted_return(const float *reward, const uint8_t *terminated,
+                           const uint8_t *truncated, const float *trunc_value,
+                           const float *bootstrap, float gamma, int64_t N, int64_t T,
+                           int64_t ld, float *returns, void *stream)
+{
+    return discounted_return(reward, terminated, truncated, trunc_value, bootstrap, gamma, N, T,
+                             ld, returns, kNoWorkspace, stream);
+}
+
+int rlca_discounted_return_ex(const float *reward, const uint8_t *terminated,
+                              const uint8_t *truncated, const float *trunc_value,
+                              const float *bootstrap, float gamma, int64_t N, int64_t T,
+                              int64_t ld, float *returns, void *workspace,
+                              size_t workspace_bytes, void *stream)
+{
+    return discounted_return(reward, terminated, truncated, trunc_value, bootstrap, gamma, N, T,
+                             ld, returns, Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_td_lambda(const float *reward, const float *value, const uint8_t *terminated,
+                   const uint8_t *truncated, const float *trunc_value,
+                   const float *bootstrap, float gamma, float lambda, int64_t N,
+                   int64_t T, int64_t ld, float *targets, void *stream)
+{
+    return td_lambda(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
+                     lambda, N, T, ld, targets, kNoWorkspace, stream);
+}
+
+int rlca_td_lambda_ex(const float *reward, const float *value, const uint8_t *terminated,
+                      const uint8_t *truncated, const float *trunc_value,
+                      const float *bootstrap, float gamma, float lambda, int64_t N,
+                      int64_t T, int64_t ld, float *targets, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    return td_lambda(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
+                     lambda, N, T, ld, targets, Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_gae(const float *reward, const float *value, const uint8_t *terminated,
+             const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+             float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+             float *advantages, float *returns, void *stream)
+{
+    return gae(reward, value, terminated, truncated, trunc_value, bootstrap, gamma, lambda, N,
+               T, ld, advantages, returns, kNoWorkspace, stream);
+}
+
+int rlca_gae_ex(const float *reward, const float *value, const uint8_t *terminated,
+                const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+                float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+                float *advantages, float *returns, void *workspace, size_t workspace_bytes,
+                void *stream)
+{
+    return gae(reward, value, terminated, truncated, trunc_value, bootstrap, gamma, lambda, N,
+               T, ld, advantages, returns, Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
+                const uint8_t *terminated, const uint8_t *truncated,
+                const float *trunc_value, const float *bootstrap, float gamma,
+                float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream)
+{
+    return vtrace(reward, value, log_rho, terminated, truncated, trunc_value, bootstrap, gamma,
+                  lambda, rho_bar, c_bar, pg_rho_bar, N, T, ld, vs, pg_advantages,
+                  kNoWorkspace, stream);
+}
+
+int rlca_vtrace_ex(const float *reward, const float *value, const float *log_rho,
+                   const uint8_t *terminated, const uint8_t *truncated,
+                   const float *trunc_value, const float *bootstrap, float gamma,
+                   float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                   int64_t T, int64_t ld, float *vs, float *pg_advantages, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    return vtrace(reward, value, log_rho, terminated, truncated, trunc_value, bootstrap, gamma,
+                  lambda, rho_bar, c_bar, pg_rho_bar, N, T, ld, vs, pg_advantages,
+                  Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_retrace(const float *reward, const float *q_taken, const float *expected_q,
+                 const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+                 const float *trunc_value, const float *bootstrap_ev, float gamma,
+                 float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                 void *stream)
+{
+    return retrace(reward, q_taken, expected_q, rho, terminated, truncated, trunc_value,
+                   bootstrap_ev, gamma, lambda, N, T, ld, q_ret, kNoWorkspace, stream);
+}
+
+int rlca_retrace_ex(const float *reward, const float *q_taken, const float *expected_q,
+                    const float *rho, const uint8_t *terminated, const uint8_t *truncated,
+                    const float *trunc_value, const float *bootstrap_ev, float gamma,
+                    float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    return retrace(reward, q_taken, expected_q, rho, terminated, truncated, trunc_value,
+                   bootstrap_ev, gamma, lambda, N, T, ld, q_ret,
+                   Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, int64_t N,
+                                int64_t T, float *returns, void *workspace,
+                                size_t workspace_bytes, int spin_limit, void *stream)
+{
+    if (!workspace || rlca::workspace_bytes(N, T) == 0 || spin_limit <= 0)
+        return RLCA_ERR_WORKSPACE;
+    return discounted_return(reward, terminated, nullptr, nullptr, nullptr, 0.99f, N, T, T,
+                             returns, Workspace{workspace, workspace_bytes}, stream, spin_limit,
+                             1);
 }
 
 }  // extern "C"

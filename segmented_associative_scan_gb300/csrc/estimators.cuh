@@ -52,6 +52,10 @@ struct Params {
     int rows_per_tile;
     int chunks_per_row;
     int segs;
+    // Decoupled look-back across the tiles of a row (kernels.cuh, Tiling::kLookback).
+    void *ws;         // caller-owned workspace: header + one 32-byte state per tile
+    int spin_limit;   // consecutive empty polls of a later tile before giving up
+    int stall;        // testing only: nonzero = tiles never publish their state
 };
 
 template <Est E>

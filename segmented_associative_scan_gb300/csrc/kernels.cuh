@@ -9,35 +9,145 @@
 // combined through shared memory. Each thread then replays its own items from its
 // carry-in, so every A_t comes out of registers and is written once.
 //
-// Two tilings of the [N, T] rollout:
-//   kRows     (T <= NT*ITEMS): a tile holds rows_per_tile whole rows, each padded to a
-//             multiple of ITEMS. Every row ends in a reset at t = T-1, so tiles are
-//             independent and no carry crosses a tile.
-//   kRowLoop  (T > NT*ITEMS): one CTA per row walks the row's segs tiles from the last
-//             to the first, carrying A at the first step of the later tile in registers.
-//             Only one tile is on chip at a time, so long sequences never exhaust
-//             registers or shared memory (the register-pressure limit the pages report
-//             for Retrace at T > 2048 does not arise).
+// Three tilings of the [N, T] rollout:
+//   kRows      (T <= NT*ITEMS): a tile holds rows_per_tile whole rows, each padded to a
+//              multiple of ITEMS. Every row ends in a reset at t = T-1, so tiles are
+//              independent and no carry crosses a tile.
+//   kRowLoop   (T > NT*ITEMS): one CTA per row walks the row's segs tiles from the last
+//              to the first, carrying A at the first step of the later tile in registers.
+//              Only one tile is on chip at a time, so long sequences never exhaust
+//              registers or shared memory (the register-pressure limit the pages report
+//              for Retrace at T > 2048 does not arise).
+//   kLookback  (T > NT*ITEMS, caller workspace): one CTA per tile, all tiles of all rows
+//              in flight at once. A tile's carry-in comes from the later tiles of its row
+//              by decoupled look-back (Merrill & Garland 2016, run towards larger t):
+//              each tile publishes its aggregate, then its inclusive value (A at its
+//              first step) once known; a tile folds later aggregates until it meets an
+//              inclusive value. A tile whose aggregate contains a reset knows its
+//              inclusive value at once, so look-back never passes an episode boundary.
 #pragma once
 
 #include "estimators.cuh"
 
 namespace rlca {
 
-enum class Tiling : int { kRows = 0, kRowLoop = 1 };
+enum class Tiling : int { kRows = 0, kRowLoop = 1, kLookback = 2 };
 
 template <int NT>
 struct ScanSmem {
     float a[2][NT / 32];
     float b[2][NT / 32];
     int f[2][NT / 32];
+    float carry;
+    unsigned tile;
+    unsigned epoch;
 };
 
-// One tile: scan the steps this thread owns, given the tile's carry-in (A at the step
-// after the tile), write the outputs and return A at the tile's first step.
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC>
+// ------------------------------------------------------------------ look-back state
+
+// Workspace: a 256-byte header, then one 32-byte state per tile (row-major over
+// [N, segs]). A state word packs a float value (high 32 bits) with a tag (low 32 bits):
+// tag = epoch * 4 + kind, kind 1 = aggregate alpha, 2 = aggregate beta, 3 = inclusive.
+// The epoch advances once per launch, so states left by earlier launches never match
+// and the workspace needs zeroing only once, before its first use.
+struct LookbackHeader {
+    unsigned epoch;         // launches completed on this workspace (mod 2^30)
+    unsigned tile_counter;  // next virtual tile id of the running launch
+    unsigned done_counter;  // CTAs of the running launch that have finished
+    int error;              // 0, or RLCA_ERR_TIMEOUT (-7) after a wait gave up
+};
+constexpr int kWsHeaderBytes = 256;
+constexpr int kTileStateBytes = 32;
+constexpr unsigned kEpochMask = 0x3fffffffu;
+constexpr int kErrTimeout = -7;
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long pack(float v, unsigned tag)
+{
+    return ((unsigned long long)__float_as_uint(v) << 32) | tag;
+}
+
+__device__ __forceinline__ float unpack_value(unsigned long long w)
+{
+    return __uint_as_float((unsigned)(w >> 32));
+}
+
+__device__ __forceinline__ unsigned long long *tile_state(void *ws, int64_t tile)
+{
+    return reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kWsHeaderBytes +
+                                                  tile * kTileStateBytes);
+}
+
+// Run by one thread: publish this tile's aggregate, find its carry-in from the later
+// tiles of the row, publish its inclusive value, return the carry-in.
+__device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, int seg, unsigned epoch,
+                                const Affine &tot)
+{
+    const unsigned tag_a = epoch * 4u + 1u, tag_b = epoch * 4u + 2u, tag_p = epoch * 4u + 3u;
+    unsigned long long *me = tile_state(p.ws, row * p.segs + seg);
+    const bool publish = p.stall == 0;
+    if (seg == p.segs - 1) {  // the row's last tile ends in a reset at t = T-1
+        if (publish) st_relaxed(me + 2, pack(affine_apply(tot, 0.f), tag_p));
+        return 0.f;
+    }
+    if (publish) {
+        if (tot.f) {
+            st_relaxed(me + 2, pack(tot.a, tag_p));
+        } else {
+            st_relaxed(me + 0, pack(tot.a, tag_a));
+            st_relaxed(me + 1, pack(tot.b, tag_b));
+        }
+    }
+    Affine acc = affine_identity();
+    float carry = 0.f;
+    int j = seg + 1;
+    int idle = 0;
+    while (true) {
+        unsigned long long *st = tile_state(p.ws, row * p.segs + j);
+        const unsigned long long wp = ld_relaxed(st + 2);
+        if ((unsigned)wp == tag_p) {
+            carry = affine_apply(acc, unpack_value(wp));
+            break;
+        }
+        const unsigned long long wa = ld_relaxed(st + 0);
+        const unsigned long long wb = ld_relaxed(st + 1);
+        if ((unsigned)wa == tag_a && (unsigned)wb == tag_b) {
+            acc = affine_compose(acc, Affine{unpack_value(wa), unpack_value(wb), 0});
+            ++j;  // the row's last tile always publishes an inclusive value: j < segs
+            idle = 0;
+            continue;
+        }
+        if (++idle > p.spin_limit) {  // bounded wait: report, never hang
+            atomicExch(&static_cast<LookbackHeader *>(p.ws)->error, kErrTimeout);
+            carry = __int_as_float(0x7fc00000);  // NaN marks this tile's outputs
+            break;
+        }
+        __nanosleep(idle < 64 ? 32 : 256);
+    }
+    if (publish && !tot.f) st_relaxed(me + 2, pack(affine_apply(tot, carry), tag_p));
+    return carry;
+}
+
+// ------------------------------------------------------------------------- one tile
+
+// Scan the steps this thread owns, write the outputs and return A at the tile's first
+// step. The tile's carry-in (A at the step after the tile) is `carry_in`, or, with LB,
+// the result of the look-back (`epoch` and `seg` identify the tile's state).
+template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB>
 __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
-                                           float carry_in, ScanSmem<NT> &sm, int buf)
+                                           float carry_in, ScanSmem<NT> &sm, int buf,
+                                           int seg = 0, unsigned epoch = 0)
 {
     constexpr int NW = NT / 32;
     const int lane = threadIdx.x & 31;
@@ -64,20 +174,38 @@ __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0,
     }
     __syncthreads();
 
-    // A at the step after this warp: later warps applied to the tile carry-in.
-    float x = carry_in;
+    if (LB) {
+        if (threadIdx.x == 0) {
+            Affine tot = Affine{sm.a[buf][0], sm.b[buf][0], sm.f[buf][0]};
 #pragma unroll
-    for (int w = NW - 1; w >= 0; --w)
-        if (w > warp) x = affine_apply(Affine{sm.a[buf][w], sm.b[buf][w], sm.f[buf][w]}, x);
-    const float a_after = affine_apply(excl, x);
+            for (int w = 1; w < NW; ++w)
+                tot = affine_compose(tot, Affine{sm.a[buf][w], sm.b[buf][w], sm.f[buf][w]});
+            sm.carry = lookback_carry(p, row, seg, epoch, tot);
+        }
+        __syncthreads();
+        carry_in = sm.carry;
+    }
 
-    // A at the tile's first step: continue through this warp and the earlier ones.
-    float tile_first = x;
+    // Combine the NW warp totals with a suffix scan over lanes 0..NW-1 of every warp:
+    // lane w ends with S_w = total_w (+) ... (+) total_{NW-1}.
+    Affine tw = affine_identity();
+    if (lane < NW) tw = Affine{sm.a[buf][lane], sm.b[buf][lane], sm.f[buf][lane]};
 #pragma unroll
-    for (int w = NW - 1; w >= 0; --w)
-        if (w <= warp)
-            tile_first =
-                affine_apply(Affine{sm.a[buf][w], sm.b[buf][w], sm.f[buf][w]}, tile_first);
+    for (int d = 1; d < NW; d <<= 1) {
+        Affine y = shfl_down(tw, d);
+        if (lane + d < NW) tw = affine_compose(tw, y);
+    }
+    // A at the step after this warp is S_{warp+1} applied to the tile carry-in; A at the
+    // tile's first step is S_0 applied to it.
+    Affine later = Affine{__shfl_sync(kFullMask, tw.a, warp + 1),
+                          __shfl_sync(kFullMask, tw.b, warp + 1),
+                          __shfl_sync(kFullMask, tw.f, warp + 1)};
+    if (warp == NW - 1) later = affine_identity();
+    const Affine whole = Affine{__shfl_sync(kFullMask, tw.a, 0), __shfl_sync(kFullMask, tw.b, 0),
+                                __shfl_sync(kFullMask, tw.f, 0)};
+    const float x = affine_apply(later, carry_in);
+    const float a_after = affine_apply(excl, x);
+    const float tile_first = affine_apply(whole, carry_in);
 
     float A[ITEMS];
     A[ITEMS - 1] = affine_apply(e[ITEMS - 1], a_after);
@@ -91,19 +219,46 @@ template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
 __global__ void __launch_bounds__(NT) credit_scan_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
+    constexpr int TILE = NT * ITEMS;
     if (TL == Tiling::kRows) {
         const int local_row = threadIdx.x / p.chunks_per_row;
         const int chunk = threadIdx.x - local_row * p.chunks_per_row;
         const int64_t row = (int64_t)blockIdx.x * p.rows_per_tile + local_row;
         const bool active = local_row < p.rows_per_tile && row < p.N;
-        scan_tile<E, NT, ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f, sm, 0);
-    } else {
-        constexpr int TILE = NT * ITEMS;
+        scan_tile<E, NT, ITEMS, VEC, TRUNC, false>(p, row, chunk * ITEMS, active, 0.f, sm, 0);
+    } else if (TL == Tiling::kRowLoop) {
         const int64_t row = blockIdx.x;
         float carry = 0.f;
         for (int s = p.segs - 1; s >= 0; --s)
-            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC>(p, row, s * TILE + threadIdx.x * ITEMS,
-                                                        true, carry, sm, s & 1);
+            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false>(
+                p, row, s * TILE + threadIdx.x * ITEMS, true, carry, sm, s & 1);
+    } else {
+        LookbackHeader *h = static_cast<LookbackHeader *>(p.ws);
+        if (threadIdx.x == 0) {
+            // Virtual tile ids in start order; a row's later tiles get smaller ids, so
+            // every tile waits only on tiles whose CTAs started before it.
+            sm.tile = atomicAdd(&h->tile_counter, 1u);
+            sm.epoch = *reinterpret_cast<volatile unsigned *>(&h->epoch);
+        }
+        __syncthreads();
+        const unsigned vid = sm.tile;
+        const unsigned epoch = sm.epoch;
+        const int64_t row = vid / (unsigned)p.segs;
+        const int seg = p.segs - 1 - (int)(vid - row * p.segs);
+        scan_tile<E, NT, ITEMS, VEC, TRUNC, true>(p, row, seg * TILE + threadIdx.x * ITEMS,
+                                                  true, 0.f, sm, 0, seg, epoch);
+        // The last CTA to finish rearms the workspace for the next launch.
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned done = atomicAdd(&h->done_counter, 1u);
+            if (done == gridDim.x - 1) {
+                h->tile_counter = 0;
+                h->done_counter = 0;
+                h->epoch = (epoch + 1u) & kEpochMask;
+                __threadfence();
+            }
+        }
     }
 }
 

@@ -72,9 +72,11 @@ class Placed:
 
 
 def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0",
-            check_guards=True, drop_second_output=False):
-    """Run `est` on the CUDA path; returns {output name: float64 array}."""
+            check_guards=True, drop_second_output=False, workspace=None):
+    """Run `est` on the CUDA path; returns {output name: float64 array}. `workspace`
+    (a zeroed uint8 CUDA tensor) selects the look-back (_ex) entry point."""
     N, T = ro.N, ro.T
+    ws = dict(workspace=workspace)
     ld = T if ld is None else ld
     p = dict(DEFAULT_PARAMS[est], **params)
 
@@ -99,23 +101,23 @@ def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0
     o = lambda name: v(outs.get(name))
     if est == "return":
         rlca.rlca_discounted_return(r.view, **fl, bootstrap=boot, gamma=p["gamma"],
-                                    returns=o("returns"))
+                                    returns=o("returns"), **ws)
     elif est == "td_lambda":
         rlca.rlca_td_lambda(r.view, f32(ro.value).view, **fl, bootstrap=boot,
-                            gamma=p["gamma"], lam=p["lam"], targets=o("targets"))
+                            gamma=p["gamma"], lam=p["lam"], targets=o("targets"), **ws)
     elif est == "gae":
         rlca.rlca_gae(r.view, f32(ro.value).view, **fl, bootstrap=boot, gamma=p["gamma"],
                       lam=p["lam"], advantages=o("advantages"), returns=o("returns"),
-                      want_returns=False)
+                      want_returns=False, **ws)
     elif est == "vtrace":
         rlca.rlca_vtrace(r.view, f32(ro.value).view, f32(ro.log_rho).view, **fl,
                          bootstrap=boot, gamma=p["gamma"], lam=p["lam"], rho_bar=p["rho_bar"],
                          c_bar=p["c_bar"], pg_rho_bar=p["pg_rho_bar"], vs=o("vs"),
-                         pg_advantages=o("pg_advantages"), want_pg=False)
+                         pg_advantages=o("pg_advantages"), want_pg=False, **ws)
     else:
         rlca.rlca_retrace(r.view, f32(ro.q_taken).view, f32(ro.expected_q).view,
                           f32(ro.rho).view, **fl, bootstrap_ev=boot, gamma=p["gamma"],
-                          lam=p["lam"], q_ret=o("q_ret"))
+                          lam=p["lam"], q_ret=o("q_ret"), **ws)
     torch.cuda.synchronize()
     if check_guards:
         for name, pl in outs.items():

@@ -107,3 +107,22 @@ def test_aliasing(lib):
     assert lib.rlca_gae(*gae_args(adv=fake(3) - 16)) == ALIAS  # runs into the flags
     assert lib.rlca_discounted_return(fake(1), fake(2), None, None, fake(3), 0.9, N, T, T,
                                       fake(3) - 8, None) == ALIAS  # overlaps bootstrap
+
+
+def test_workspace_size_and_validation(lib):
+    assert lib.rlca_workspace_bytes(4, 1024) == 0
+    assert lib.rlca_workspace_bytes(4, 1025) == 256 + 32 * 4 * 2
+    assert lib.rlca_workspace_bytes(2048, 4096) == 256 + 32 * 2048 * 4
+    assert lib.rlca_workspace_bytes(-1, 5000) == 0
+    N, T = 4, 2048
+    need = lib.rlca_workspace_bytes(N, T)
+    ws = 0x40000000
+    args = lambda w, nb: (fake(1), fake(2), fake(3), None, None, None, 0.99, 0.95, N, T, T,
+                          fake(4), fake(5), w, nb, None)
+    assert lib.rlca_gae_ex(*args(ws, need - 1)) == WORKSPACE
+    assert lib.rlca_gae_ex(*args(ws + 16, need)) == WORKSPACE  # not 256-byte aligned
+    assert lib.rlca_gae_ex(*args(fake(1), need)) == ALIAS     # overlaps an input
+    assert lib.rlca_gae_ex(*args(fake(4), need)) == ALIAS     # overlaps an output
+    assert lib.rlca_testing_lookback_stall(fake(1), fake(2), 4, 1000, fake(3), ws, 10**6, 8,
+                                           None) == WORKSPACE  # one tile per row
+    assert lib.rlca_workspace_check(None, None) == NULL
