@@ -156,6 +156,27 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+# --------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, dist) -> float:
+    """The largest `value` over all ranks (host-side timing only; the data path has no
+    collective). NCCL reduces a CUDA tensor, gloo a CPU one."""
+    if dist is None:
+        return value
+    import torch
+    on_gpu = dist.get_backend() == "nccl"
+    dev = torch.device("cuda", torch.cuda.current_device()) if on_gpu else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, N: int, T: int, steps: int, ms_max: float) -> float:
+    """Whole-job timesteps/s: every rank processed its own batch each step (weak
+    scaling), and the job took as long as its slowest rank."""
+    return world * N * T * steps / (ms_max * 1e-3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 class DeviceSet:
@@ -371,17 +392,13 @@ def gpu_arm(args, rank, world, local_rank, dist):
     sampler.stop()
     clocks = sampler.summary(t0, t1)
 
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist)
     if rank != 0:
         return None
 
     launch_us = 1000.0 * ms / K
     achieved = kernel_bytes_per_step / (launch_us * 1e-6) / 1e9
-    value = world * N_ENVS * SEQ_LEN * K / (ms_max * 1e-3)
+    value = job_throughput(world, N_ENVS, SEQ_LEN, K, ms_max)
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(src_hash)
     result = {
