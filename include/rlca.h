@@ -218,6 +218,32 @@ int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, 
                                 int64_t T, float *returns, void *workspace,
                                 size_t workspace_bytes, int spin_limit, void *stream);
 
+/*
+ * GAE that allocates nothing, for callers that cannot allocate device memory: code
+ * that a host framework hands only its input and output buffers (the framework plans
+ * all device memory itself), or a loop running under a fixed memory budget where a
+ * cudaMalloc could fail or stall the device. The paper has no counterpart to this
+ * entry point.
+ *
+ * Same arguments, results and errors as rlca_gae. When T > 1024 it runs the look-back
+ * path of rlca_gae_ex on a workspace the library keeps in a static device array of
+ * 256 + 32 * RLCA_NOALLOC_MAX_TILES bytes (about 1 MiB), which every GPU that loads the
+ * library holds until the process exits. Limit: N * ceil(T / 1024) <= RLCA_NOALLOC_MAX_TILES,
+ * else RLCA_ERR_WORKSPACE and nothing is enqueued. It calls no allocator.
+ *   - The first call on each device sets the array up (looks up its device address with
+ *     that device current and zeroes it, synchronously). Make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps the previous
+ *     call's contents (each call clears the parts that must start at zero). Calls whose
+ *     kernels overlap on the GPU race on it: issue them on one stream, or order them.
+ *   - A look-back wait that gives up marks the affected outputs NaN.
+ */
+#define RLCA_NOALLOC_MAX_TILES 32768
+int rlca_gae_noalloc(const float *reward, const float *value, const uint8_t *terminated,
+                     const uint8_t *truncated, const float *trunc_value,
+                     const float *bootstrap, float gamma, float lambda, int64_t N, int64_t T,
+                     int64_t ld, float *advantages, float *returns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -44,6 +44,7 @@ SIGNATURES = {
     "rlca_testing_lookback_stall": ([_P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, ctypes.c_int,
                                      _P], ctypes.c_int),
 }
+SIGNATURES["rlca_gae_noalloc"] = SIGNATURES["rlca_gae"]
 # The _ex variants take (workspace, workspace_bytes) before the stream.
 for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
               "rlca_retrace"):
