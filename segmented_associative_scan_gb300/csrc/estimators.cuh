@@ -4,7 +4,8 @@
 // inputs and are never written to memory).
 //
 // Each thread owns ITEMS consecutive steps t0 .. t0+ITEMS-1 of one env row. For every
-// step it forms (alpha_t, beta_t, reset_t) of A_t = alpha_t + beta_t * A_{t+1}:
+// step it forms (alpha_t, beta_t) of A_t = alpha_t + beta_t * A_{t+1}, with beta < 0
+// marking a reset (scan_core.cuh):
 //
 //   estimator   alpha_t                                       beta_t          output
 //   return      r_t (+ gamma * sv_t if the episode stops)     gamma           G = A
@@ -17,7 +18,8 @@
 // where sv_t (successor value, Method section 3) is 0 for a terminated step, the
 // supplied truncation value for a truncated one and the per-env bootstrap at t = T-1;
 // V(s_{t+1}) / EQ(s_{t+1}) is V_{t+1} / E_pi Q_{t+1} inside an episode and sv_t at its
-// last step; reset_t is set exactly at an episode's last step.
+// last step, where the step resets. Every step is first built as if its episode went
+// on; the few steps where an episode stops are then patched.
 #pragma once
 
 #include "scan_core.cuh"
@@ -78,9 +80,11 @@ struct Chunk {
     float v[ITEMS];
     float x[ITEMS];
     float y[ITEMS];
-    float sv[ITEMS];  // successor value at steps where the episode stops
+    float sv[ITEMS];  // successor value where the episode stops (V-trace keeps it)
     float v_next, x_next, y_next;
     unsigned stop;   // bit j: the recursion stops at step j (boundary or padding)
+    unsigned term;   // bit j: step j terminated
+    unsigned trunc;  // bit j: step j truncated
     unsigned valid;  // bit j: step t0+j exists in this row
 };
 
@@ -107,37 +111,17 @@ __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0,
     if (Tr::kValue) load_items<ITEMS, VEC>(p.value + off, t0, Te, c.v);
     if (Tr::kAux) load_items<ITEMS, VEC>(p.aux + off, t0, Te, c.x);
     if (Tr::kRho) load_items<ITEMS, VEC>(p.rho + off, t0, Te, c.y);
-    const unsigned term = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
-    const unsigned trunc = TRUNC ? load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te) : 0u;
-
-    unsigned valid = 0;
-#pragma unroll
-    for (int j = 0; j < ITEMS; ++j) valid |= (t0 + j < Te ? 1u : 0u) << j;
+    c.term = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
+    c.trunc = TRUNC ? load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te) : 0u;
+    c.valid = valid_items<ITEMS>(t0, Te);
     const int last = T - 1 - t0;
     const unsigned window_end = (last >= 0 && last < ITEMS) ? (1u << last) : 0u;
-    const unsigned all = (ITEMS == 32) ? 0xffffffffu : ((1u << ITEMS) - 1u);
-    c.valid = valid;
-    c.stop = (term | trunc | window_end | ~valid) & all;
+    c.stop = (c.term | c.trunc | window_end | ~c.valid) & all_items<ITEMS>();
 
     const bool need = active && (t0 + ITEMS < T);
     if (Tr::kNextValue) c.v_next = next_item(c.v[0], p.value + off, t0 + ITEMS, need, lane);
     if (Tr::kNextAux) c.x_next = next_item(c.x[0], p.aux + off, t0 + ITEMS, need, lane);
     if (Tr::kNextRho) c.y_next = next_item(c.y[0], p.rho + off, t0 + ITEMS, need, lane);
-
-    // Successor values where an episode stops (Method section 3): termination 0, then
-    // truncation (value read only where truncated), then the window-end bootstrap.
-#pragma unroll
-    for (int j = 0; j < ITEMS; ++j) {
-        float s = 0.f;
-        const unsigned bit = 1u << j;
-        if ((valid & bit) && !(term & bit)) {
-            if (trunc & bit)
-                s = __ldg(p.trunc_value + off + t0 + j);
-            else if (window_end & bit)
-                s = p.boot ? __ldg(p.boot + row) : 0.f;
-        }
-        c.sv[j] = s;
-    }
 }
 
 template <int ITEMS>
@@ -146,42 +130,66 @@ __device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next,
     return (j + 1 < ITEMS) ? a[j + 1] : next;
 }
 
-// Forms (alpha, beta, reset) of every item. V-trace keeps rho_t in c.x for the epilogue.
-template <Est E, int ITEMS>
-__device__ __forceinline__ void build(const Params &p, Chunk<ITEMS> &c, Affine (&e)[ITEMS])
+// alpha of one step given the value of the state after it (`nxt`).
+template <Est E>
+__device__ __forceinline__ float alpha_of(const Params &p, float r, float v, float rho_hat,
+                                          float nxt)
 {
+    if (E == Est::kReturn || E == Est::kTdLambda) return fmaf(p.gamma, nxt, r);
+    if (E == Est::kVtrace) return rho_hat * (fmaf(p.gamma, nxt, r) - v);
+    return fmaf(p.gamma, nxt, r) - v;  // GAE delta; Retrace with v = Q_t
+}
+
+// Forms (alpha, beta) of every item. V-trace keeps rho_t in c.x for the epilogue.
+template <Est E, int ITEMS>
+__device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chunk<ITEMS> &c,
+                                      Affine (&e)[ITEMS])
+{
+    float rho_hat[ITEMS];
 #pragma unroll
     for (int j = 0; j < ITEMS; ++j) {
-        const bool stop = (c.stop >> j) & 1u;
         const float r = c.r[j];
-        float a, b;
+        rho_hat[j] = 1.f;
         if (E == Est::kReturn) {
-            a = stop ? fmaf(p.gamma, c.sv[j], r) : r;
-            b = p.gamma;
+            e[j] = Affine{r, p.gamma};
         } else if (E == Est::kTdLambda) {
-            a = stop ? fmaf(p.gamma, c.sv[j], r)
-                     : fmaf(p.gamma_one_m_lambda, at_or_next(c.v, c.v_next, j), r);
-            b = p.gamma_lambda;
+            e[j] = Affine{fmaf(p.gamma_one_m_lambda, at_or_next(c.v, c.v_next, j), r),
+                          p.gamma_lambda};
         } else if (E == Est::kGae) {
-            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
-            a = fmaf(p.gamma, nxt, r) - c.v[j];
-            b = p.gamma_lambda;
+            e[j] = Affine{alpha_of<E>(p, r, c.v[j], 0.f, at_or_next(c.v, c.v_next, j)),
+                          p.gamma_lambda};
         } else if (E == Est::kVtrace) {
             const float rho = expf(c.x[j]);
             c.x[j] = rho;
-            const float rho_hat = rho < p.rho_bar ? rho : p.rho_bar;
+            rho_hat[j] = rho < p.rho_bar ? rho : p.rho_bar;
             const float cc = p.lambda * (rho < p.c_bar ? rho : p.c_bar);
-            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
-            a = rho_hat * (fmaf(p.gamma, nxt, r) - c.v[j]);
-            b = p.gamma * cc;
-        } else {  // Retrace
+            e[j] = Affine{alpha_of<E>(p, r, c.v[j], rho_hat[j], at_or_next(c.v, c.v_next, j)),
+                          p.gamma * cc};
+        } else {  // Retrace: beta_t uses the trace of step t+1
             const float rho1 = at_or_next(c.y, c.y_next, j);
             const float c1 = p.lambda * (rho1 < 1.f ? rho1 : 1.f);
-            const float nxt = stop ? c.sv[j] : at_or_next(c.x, c.x_next, j);
-            a = fmaf(p.gamma, nxt, r) - c.v[j];
-            b = p.gamma * c1;
+            e[j] = Affine{alpha_of<E>(p, r, c.v[j], 0.f, at_or_next(c.x, c.x_next, j)),
+                          p.gamma * c1};
         }
-        e[j] = Affine{a, b, stop ? 1 : 0};
+        c.sv[j] = 0.f;
+    }
+    if (c.stop) {
+        // Steps where the episode stops (Method section 3): successor value 0 if
+        // terminated, the truncation value if truncated (read only there), else the
+        // window-end bootstrap; the step resets. Padding items reset with value 0.
+        const int64_t off = row * p.ld;
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+            const unsigned bit = 1u << j;
+            if (c.stop & bit) {
+                float sv = 0.f;
+                if ((c.valid & bit) && !(c.term & bit))
+                    sv = (c.trunc & bit) ? __ldg(p.trunc_value + off + t0 + j)
+                                         : (p.boot ? __ldg(p.boot + row) : 0.f);
+                c.sv[j] = sv;
+                e[j] = Affine{alpha_of<E>(p, c.r[j], c.v[j], rho_hat[j], sv), kResetB};
+            }
+        }
     }
 }
 

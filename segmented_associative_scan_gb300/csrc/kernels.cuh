@@ -37,7 +37,6 @@ template <int NT>
 struct ScanSmem {
     float a[2][NT / 32];
     float b[2][NT / 32];
-    int f[2][NT / 32];
     float carry;
     unsigned tile;
     unsigned epoch;
@@ -101,8 +100,9 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
         if (publish) st_relaxed(me + 2, pack(affine_apply(tot, 0.f), tag_p));
         return 0.f;
     }
+    const bool tot_reset = is_reset(tot.b);
     if (publish) {
-        if (tot.f) {
+        if (tot_reset) {
             st_relaxed(me + 2, pack(tot.a, tag_p));
         } else {
             st_relaxed(me + 0, pack(tot.a, tag_a));
@@ -123,7 +123,7 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
         const unsigned long long wa = ld_relaxed(st + 0);
         const unsigned long long wb = ld_relaxed(st + 1);
         if ((unsigned)wa == tag_a && (unsigned)wb == tag_b) {
-            acc = affine_compose(acc, Affine{unpack_value(wa), unpack_value(wb), 0});
+            acc = affine_compose(acc, Affine{unpack_value(wa), unpack_value(wb)});
             ++j;  // the row's last tile always publishes an inclusive value: j < segs
             idle = 0;
             continue;
@@ -135,7 +135,7 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
         }
         __nanosleep(idle < 64 ? 32 : 256);
     }
-    if (publish && !tot.f) st_relaxed(me + 2, pack(affine_apply(tot, carry), tag_p));
+    if (publish && !tot_reset) st_relaxed(me + 2, pack(affine_apply(tot, carry), tag_p));
     return carry;
 }
 
@@ -156,7 +156,7 @@ __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0,
     Chunk<ITEMS> c;
     load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
     Affine e[ITEMS];
-    build<E, ITEMS>(p, c, e);
+    build<E, ITEMS>(p, row, t0, c, e);
 
     // Thread aggregate: e_0 (+) e_1 (+) ... (+) e_{ITEMS-1}.
     Affine agg = e[ITEMS - 1];
@@ -170,16 +170,15 @@ __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0,
     if (lane == 0) {
         sm.a[buf][warp] = incl.a;
         sm.b[buf][warp] = incl.b;
-        sm.f[buf][warp] = incl.f;
     }
     __syncthreads();
 
     if (LB) {
         if (threadIdx.x == 0) {
-            Affine tot = Affine{sm.a[buf][0], sm.b[buf][0], sm.f[buf][0]};
+            Affine tot = Affine{sm.a[buf][0], sm.b[buf][0]};
 #pragma unroll
             for (int w = 1; w < NW; ++w)
-                tot = affine_compose(tot, Affine{sm.a[buf][w], sm.b[buf][w], sm.f[buf][w]});
+                tot = affine_compose(tot, Affine{sm.a[buf][w], sm.b[buf][w]});
             sm.carry = lookback_carry(p, row, seg, epoch, tot);
         }
         __syncthreads();
@@ -189,20 +188,17 @@ __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0,
     // Combine the NW warp totals with a suffix scan over lanes 0..NW-1 of every warp:
     // lane w ends with S_w = total_w (+) ... (+) total_{NW-1}.
     Affine tw = affine_identity();
-    if (lane < NW) tw = Affine{sm.a[buf][lane], sm.b[buf][lane], sm.f[buf][lane]};
+    if (lane < NW) tw = Affine{sm.a[buf][lane], sm.b[buf][lane]};
 #pragma unroll
     for (int d = 1; d < NW; d <<= 1) {
-        Affine y = shfl_down(tw, d);
+        const Affine y = shfl_down(tw, d);
         if (lane + d < NW) tw = affine_compose(tw, y);
     }
     // A at the step after this warp is S_{warp+1} applied to the tile carry-in; A at the
     // tile's first step is S_0 applied to it.
-    Affine later = Affine{__shfl_sync(kFullMask, tw.a, warp + 1),
-                          __shfl_sync(kFullMask, tw.b, warp + 1),
-                          __shfl_sync(kFullMask, tw.f, warp + 1)};
+    Affine later = shfl_idx(tw, (warp + 1) & 31);
     if (warp == NW - 1) later = affine_identity();
-    const Affine whole = Affine{__shfl_sync(kFullMask, tw.a, 0), __shfl_sync(kFullMask, tw.b, 0),
-                                __shfl_sync(kFullMask, tw.f, 0)};
+    const Affine whole = shfl_idx(tw, 0);
     const float x = affine_apply(later, carry_in);
     const float a_after = affine_apply(excl, x);
     const float tile_first = affine_apply(whole, carry_in);

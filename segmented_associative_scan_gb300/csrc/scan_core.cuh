@@ -4,9 +4,14 @@
 // Learning Credit Assignment": every estimator is A_t = alpha_t + beta_t * A_{t+1}, an
 // associative scan over pairs (alpha, beta) with
 //   (aB, bB) (+) (aA, bA) = (aB + bB * aA, bA * bB),   B the earlier step, A the later.
-// Method section 3 (episode boundaries) enters as an explicit reset flag: a step whose
-// episode ends there takes nothing from t+1. The flag is a select, not a multiply by 0,
+// Method section 3 (episode boundaries) enters as an explicit reset: a step whose
+// episode ends there takes nothing from t+1. The reset is a select, not a multiply by 0,
 // so a NaN or Inf in a later episode never reaches an earlier one.
+//
+// Encoding: every beta of the estimators is >= 0 (gamma >= 0, lambda in [0,1], clipped
+// ratios >= 0), so the sign bit of b is free and carries the reset. A reset element has
+// b = -1; composing a non-reset element (b >= 0) with a reset one multiplies the signs,
+// so the composite is negative, i.e. reset, too (0 * -1 = -0 keeps the sign bit).
 #pragma once
 
 #include <cstdint>
@@ -15,38 +20,38 @@
 namespace rlca {
 
 constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kResetB = -1.0f;
 
-// The map x -> a + b * x, or the constant a when f is set (an episode ends inside).
+// The map x -> a + b * x, or the constant a when b's sign bit is set (reset inside).
 struct Affine {
     float a;
     float b;
-    int f;
 };
 
-__device__ __forceinline__ Affine affine_identity() { return Affine{0.f, 1.f, 0}; }
+__device__ __forceinline__ bool is_reset(float b) { return __float_as_int(b) < 0; }
+
+__device__ __forceinline__ Affine affine_identity() { return Affine{0.f, 1.f}; }
 
 __device__ __forceinline__ float affine_apply(const Affine &e, float x)
 {
-    return e.f ? e.a : fmaf(e.b, x, e.a);
+    return is_reset(e.b) ? e.a : fmaf(e.b, x, e.a);
 }
 
 // The pages' operator: `early` applied after `late` (early covers smaller t).
 __device__ __forceinline__ Affine affine_compose(const Affine &early, const Affine &late)
 {
-    Affine r;
-    r.a = early.f ? early.a : fmaf(early.b, late.a, early.a);
-    r.b = early.f ? early.b : early.b * late.b;
-    r.f = early.f | late.f;
-    return r;
+    const bool r = is_reset(early.b);
+    return Affine{r ? early.a : fmaf(early.b, late.a, early.a), r ? early.b : early.b * late.b};
 }
 
 __device__ __forceinline__ Affine shfl_down(const Affine &x, int d)
 {
-    Affine y;
-    y.a = __shfl_down_sync(kFullMask, x.a, d);
-    y.b = __shfl_down_sync(kFullMask, x.b, d);
-    y.f = __shfl_down_sync(kFullMask, x.f, d);
-    return y;
+    return Affine{__shfl_down_sync(kFullMask, x.a, d), __shfl_down_sync(kFullMask, x.b, d)};
+}
+
+__device__ __forceinline__ Affine shfl_idx(const Affine &x, int lane)
+{
+    return Affine{__shfl_sync(kFullMask, x.a, lane), __shfl_sync(kFullMask, x.b, lane)};
 }
 
 // Inclusive suffix scan across a warp: lane i gets x_i (+) x_{i+1} (+) ... (+) x_31.
@@ -54,7 +59,7 @@ __device__ __forceinline__ Affine warp_suffix_scan(Affine x, int lane)
 {
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        Affine y = shfl_down(x, d);
+        const Affine y = shfl_down(x, d);
         if (lane + d < 32) x = affine_compose(x, y);
     }
     return x;
@@ -69,6 +74,20 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t *p) { return __ldcs
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(float *p, float v) { __stcs(p, v); }
 
+template <int ITEMS>
+__device__ __forceinline__ constexpr unsigned all_items()
+{
+    return ITEMS == 32 ? 0xffffffffu : ((1u << ITEMS) - 1u);
+}
+
+// Bit j set for the items t0 + j < T.
+template <int ITEMS>
+__device__ __forceinline__ unsigned valid_items(int t0, int T)
+{
+    const int n = T - t0;
+    return n >= ITEMS ? all_items<ITEMS>() : (n > 0 ? (1u << n) - 1u : 0u);
+}
+
 // ITEMS consecutive floats of one row starting at column t0; columns >= T read as 0.
 template <int ITEMS, bool VEC>
 __device__ __forceinline__ void load_items(const float *__restrict__ row, int t0, int T,
@@ -77,7 +96,7 @@ __device__ __forceinline__ void load_items(const float *__restrict__ row, int t0
     if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k) {
-            float4 q = ld_stream(reinterpret_cast<const float4 *>(row + t0) + k);
+            const float4 q = ld_stream(reinterpret_cast<const float4 *>(row + t0) + k);
             x[4 * k + 0] = q.x;
             x[4 * k + 1] = q.y;
             x[4 * k + 2] = q.z;
@@ -89,6 +108,16 @@ __device__ __forceinline__ void load_items(const float *__restrict__ row, int t0
     }
 }
 
+// 4 flag bytes -> 4 bits (bit i set when byte i is nonzero), branch-free: bit 7 of each
+// byte becomes "any bit set" without carries across bytes, then one multiply gathers the
+// four bit-7s into bits 24..27 (the partial products land on distinct bit positions).
+__device__ __forceinline__ unsigned nonzero_bytes(uint32_t w)
+{
+    const uint32_t hi = ((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w;
+    const uint32_t b = (hi & 0x80808080u) >> 7;
+    return (b * 0x01020408u) >> 24;
+}
+
 // Bit j set when flag byte (t0 + j) is nonzero; columns >= T read as clear.
 template <int ITEMS, bool VEC>
 __device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ row, int t0,
@@ -97,12 +126,9 @@ __device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ r
     unsigned bits = 0;
     if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
-        for (int k = 0; k < ITEMS / 4; ++k) {
-            uint32_t w = ld_stream(reinterpret_cast<const uint32_t *>(row + t0) + k);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                bits |= (((w >> (8 * i)) & 0xffu) != 0u ? 1u : 0u) << (4 * k + i);
-        }
+        for (int k = 0; k < ITEMS / 4; ++k)
+            bits |= nonzero_bytes(ld_stream(reinterpret_cast<const uint32_t *>(row + t0) + k))
+                    << (4 * k);
     } else {
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j)
@@ -116,8 +142,7 @@ template <int ITEMS, bool VEC>
 __device__ __forceinline__ void store_items(float *__restrict__ row, int t0, unsigned valid,
                                             const float (&x)[ITEMS])
 {
-    constexpr unsigned kAll = (ITEMS == 32) ? 0xffffffffu : ((1u << ITEMS) - 1u);
-    if (VEC && valid == kAll) {
+    if (VEC && valid == all_items<ITEMS>()) {
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k)
             st_stream(reinterpret_cast<float4 *>(row + t0) + k,

@@ -217,3 +217,18 @@ def test_empty_problems():
         adv, ret = rlca.rlca_gae(r, r, d)
         assert adv.shape == (N, T) and ret.shape == (N, T)
     torch.cuda.synchronize()
+
+
+def test_flag_bytes_any_nonzero_value_is_set():
+    """Flags are bytes with 0 = clear and any nonzero value = set (0x80, 0xff, 7, ...)."""
+    ro = sr.generic(6, 2100, seed=19, p_term=0.03, p_trunc=0.03)
+    rng = np.random.default_rng(3)
+    for name in ("terminated", "truncated"):
+        f = getattr(ro, name)
+        vals = rng.choice(np.array([1, 2, 7, 0x10, 0x7f, 0x80, 0x81, 0xfe, 0xff], np.uint8),
+                          size=f.shape)
+        setattr(ro, name, np.where(f != 0, vals, 0).astype(np.uint8))
+    for est in ESTIMATORS:
+        assert_parity(run_gpu(est, ro, {}), run_oracle(est, ro, {}), f"{est} flag bytes")
+        assert_parity(run_gpu(est, ro, {}, ld=2104, offset=0), run_oracle(est, ro, {}),
+                      f"{est} flag bytes, padded rows")
