@@ -41,7 +41,11 @@ L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes per launch measured by ncu for the GAE [4096,1024] kernel, keyed by a hash of
 # the kernel sources at the time of the capture; null once the kernels change.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # credit_warp_stream_kernel<GAE>: dram read 43.01 MB + write 0.98 MB in one captured
+    # launch (outputs stay in L2 within it): profiles/gae_trunc_4096x1024_warp_stream_kernel.md
+    "2e33c7daeb6c28e1": 43_991_552,
+}
 
 
 def kernel_source_hash() -> str:
@@ -419,7 +423,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": "credit_scan_kernel<GAE, whole-row tiles>",
+            "kernel": "credit_warp_stream_kernel<GAE> (warp-owned rows, per-warp TMA ring)",
             "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),
             "launch_us": round(launch_us, 3), "peak_source": peak_src,
             "frac_of_8tbs": round(achieved / 8000.0, 4), "kernel_source": src_hash},

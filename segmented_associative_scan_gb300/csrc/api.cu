@@ -101,7 +101,13 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
     for (int i = 0; i < n_in; ++i) vec = vec && aligned(f32_in[i], 16);
     for (int o = 0; o < n_out; ++o) vec = vec && (!outs[o] || aligned(outs[o], 16));
 
-    const cudaError_t err = launch(p, vec, static_cast<cudaStream_t>(stream));
+    // The warp-streaming kernel moves chunks with 16-byte bulk copies: every base
+    // 16-byte aligned, ld and T multiples of 16, and packed rows contiguous (ld == T).
+    bool streamable = vec && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
+                      (p.T > rlca::kWarpChunk || p.ld == p.T) && aligned(p.term, 16) &&
+                      (!p.trunc || aligned(p.trunc, 16));
+
+    const cudaError_t err = launch(p, vec, streamable, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? RLCA_OK : RLCA_ERR_LAUNCH;
 }
 

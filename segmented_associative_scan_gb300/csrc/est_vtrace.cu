@@ -3,8 +3,8 @@
 #include "launch.cuh"
 
 namespace rlca {
-cudaError_t launch_vtrace(const Params &p, bool vec, cudaStream_t stream)
+cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream_t stream)
 {
-    return launch_estimator<Est::kVtrace>(p, vec, stream);
+    return launch_estimator<Est::kVtrace>(p, vec, streamable, stream);
 }
 }  // namespace rlca

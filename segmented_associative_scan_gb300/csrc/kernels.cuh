@@ -31,7 +31,7 @@
 
 namespace rlca {
 
-enum class Tiling : int { kRows = 0, kRowLoop = 1, kLookback = 2 };
+enum class Tiling : int { kRows = 0, kRowLoop = 1, kLookback = 2, kWarp = 3 };
 
 template <int NT>
 struct ScanSmem {
@@ -141,20 +141,18 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
 
 // ------------------------------------------------------------------------- one tile
 
-// Scan the steps this thread owns, write the outputs and return A at the tile's first
-// step. The tile's carry-in (A at the step after the tile) is `carry_in`, or, with LB,
-// the result of the look-back (`epoch` and `seg` identify the tile's state).
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB>
-__device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
-                                           float carry_in, ScanSmem<NT> &sm, int buf,
-                                           int seg = 0, unsigned epoch = 0)
+// Scan the loaded steps this thread owns, write the outputs and return A at the tile's
+// first step. The tile's carry-in (A at the step after the tile) is `carry_in`, or,
+// with LB, the result of the look-back (`epoch` and `seg` identify the tile's state).
+template <Est E, int NT, int ITEMS, bool VEC, bool LB>
+__device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, int64_t row,
+                                            int t0, float carry_in, ScanSmem<NT> &sm, int buf,
+                                            int seg = 0, unsigned epoch = 0)
 {
     constexpr int NW = NT / 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
 
-    Chunk<ITEMS> c;
-    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
     Affine e[ITEMS];
     build<E, ITEMS>(p, row, t0, c, e);
 
@@ -211,10 +209,32 @@ __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0,
     return tile_first;
 }
 
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
-__global__ void __launch_bounds__(NT) credit_scan_kernel(const Params p)
+// Load this thread's steps from global memory, then scan_chunk.
+template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB>
+__device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
+                                           float carry_in, ScanSmem<NT> &sm, int buf,
+                                           int seg = 0, unsigned epoch = 0)
+{
+    Chunk<ITEMS> c;
+    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, threadIdx.x & 31, c);
+    return scan_chunk<E, NT, ITEMS, VEC, LB>(p, c, row, t0, carry_in, sm, buf, seg, epoch);
+}
+
+// Programmatic dependent launch: wait until the previous kernel in the stream has
+// completed and its writes are visible (a no-op when the launch has no such
+// dependency), then let the next kernel be scheduled while this one runs; that kernel
+// in turn waits for this one to complete before it touches memory.
+__device__ __forceinline__ void grid_dependency_sync()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, int MINB = 1>
+__global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
+    grid_dependency_sync();
     constexpr int TILE = NT * ITEMS;
     if (TL == Tiling::kRows) {
         const int local_row = threadIdx.x / p.chunks_per_row;
@@ -255,6 +275,63 @@ __global__ void __launch_bounds__(NT) credit_scan_kernel(const Params p)
                 __threadfence();
             }
         }
+    }
+}
+
+// ----------------------------------------------------------- warp-owned rows (kWarp)
+
+// One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
+// aggregates, a warp suffix scan, and the chunk's carry-in (A at the step after the
+// chunk) applied directly. Returns A at the chunk's first step.
+template <Est E, int ITEMS, bool VEC, bool TRUNC>
+__device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0, bool active,
+                                            float carry_in)
+{
+    const int lane = threadIdx.x & 31;
+    Chunk<ITEMS> c;
+    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
+    Affine e[ITEMS];
+    build<E, ITEMS>(p, row, t0, c, e);
+    Affine agg = e[ITEMS - 1];
+#pragma unroll
+    for (int j = ITEMS - 2; j >= 0; --j) agg = affine_compose(e[j], agg);
+    const Affine incl = warp_suffix_scan(agg, lane);
+    Affine excl = shfl_down(incl, 1);
+    if (lane == 31) excl = affine_identity();
+    const Affine whole = shfl_idx(incl, 0);
+    const float a_after = affine_apply(excl, carry_in);
+    float A[ITEMS];
+    A[ITEMS - 1] = affine_apply(e[ITEMS - 1], a_after);
+#pragma unroll
+    for (int j = ITEMS - 2; j >= 0; --j) A[j] = affine_apply(e[j], A[j + 1]);
+    epilogue<E, ITEMS, VEC>(p, c, A, a_after, row, t0);
+    return affine_apply(whole, carry_in);
+}
+
+// Every warp of the grid owns one job, with no barrier and no shared memory:
+//   T <= 32 * ITEMS: rows_per_tile whole rows (padded to a multiple of ITEMS) per warp;
+//   longer T: one row per warp, walked in chunks of 32 * ITEMS steps from the last to the
+//   first with the carry in a register.
+// All warps of a typical launch are resident at once, so each keeps its next chunk's
+// loads in flight without any cross-warp wait.
+template <Est E, int ITEMS, bool VEC, bool TRUNC, int WARPS = 4>
+__global__ void __launch_bounds__(32 * WARPS) credit_warp_kernel(const Params p)
+{
+    grid_dependency_sync();
+    constexpr int CH = 32 * ITEMS;
+    const int lane = threadIdx.x & 31;
+    const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (p.segs == 1) {
+        const int local_row = lane / p.chunks_per_row;
+        const int chunk = lane - local_row * p.chunks_per_row;
+        const int64_t row = job * p.rows_per_tile + local_row;
+        const bool active = local_row < p.rows_per_tile && row < p.N;
+        warp_chunk<E, ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f);
+    } else {
+        if (job >= p.N) return;  // the whole warp leaves together
+        float carry = 0.f;
+        for (int s = p.segs - 1; s >= 0; --s)
+            carry = warp_chunk<E, ITEMS, VEC, TRUNC>(p, job, s * CH + lane * ITEMS, true, carry);
     }
 }
 

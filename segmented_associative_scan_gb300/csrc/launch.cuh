@@ -1,23 +1,25 @@
-// Host-side launch of the fused kernels: picks the tiling from T and the load width
-// from alignment, then launches on the caller's stream.
+// Host-side launch of the fused kernels: picks the kernel from the shape, the layout and
+// whether the caller gave a look-back workspace, then launches on the caller's stream.
+//
+// Every kernel begins with griddepcontrol.wait, so it is launched with programmatic
+// stream serialization (PDL): when the previous kernel in the stream allows it, this
+// launch is scheduled while that kernel drains, and still touches no memory before it
+// has completed. With a predecessor that does not opt in, the launch behaves as usual.
 #pragma once
 
+#include <atomic>
+
 #include "kernels.cuh"
+#include "warp_stream.cuh"
 
 namespace rlca {
 
-// Threads per CTA and steps per thread of the fused kernels.
+// CTA tiles: 128 threads x 8 steps.
 constexpr int kThreads = 128;
 constexpr int kItems = 8;
 constexpr int kTile = kThreads * kItems;
-
-struct LaunchShape {
-    Tiling tiling;
-    unsigned grid;
-    int rows_per_tile;
-    int chunks_per_row;
-    int segs;
-};
+// Warp-owned rows: 4 independent warps per CTA, 32 lanes x 8 steps per chunk.
+constexpr int kWarpsPerCta = 4;
 
 // Look-back tiles of an [N, T] problem (0 when T fits one tile: no look-back needed).
 inline int64_t lookback_tiles(int64_t N, int64_t T)
@@ -35,63 +37,170 @@ inline size_t workspace_bytes(int64_t N, int64_t T)
 // sleeps up to 256 ns, so about a second) before the launch reports RLCA_ERR_TIMEOUT.
 constexpr int kDefaultSpinLimit = 1 << 22;
 
-inline LaunchShape plan_launch(int64_t N, int T, bool lookback)
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, const Params &p)
 {
-    LaunchShape s{};
-    if (T <= kTile) {
-        const int t_pad = (T + kItems - 1) / kItems * kItems;
-        s.tiling = Tiling::kRows;
-        s.chunks_per_row = t_pad / kItems;
-        s.rows_per_tile = kTile / t_pad;
-        s.segs = 1;
-        s.grid = (unsigned)((N + s.rows_per_tile - 1) / s.rows_per_tile);
-    } else {
-        s.chunks_per_row = kTile / kItems;
-        s.rows_per_tile = 1;
-        s.segs = (T + kTile - 1) / kTile;
-        s.tiling = lookback ? Tiling::kLookback : Tiling::kRowLoop;
-        s.grid = (unsigned)(lookback ? N * s.segs : N);
-    }
-    return s;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
+
+// ------------------------------------------------------------------ kernel choice
+
+enum class Path : int { kCtaRows, kCtaRowLoop, kLookback, kWarpRows, kWarpStream };
+
+// Measured on GB300 (see the design notes): rows of at most one warp chunk (256 steps)
+// go to warp-owned rows, which need no CTA barrier; up to one CTA tile (1024 steps) the
+// CTA tile kernel, which loads a whole row at once, wins for every estimator but GAE,
+// whose extra flag stream makes the barrier-free warp-streaming kernel faster; longer
+// rows loop over CTA tiles (or use look-back with a workspace).
+template <Est E>
+inline Path choose_path(int64_t N, int T, bool vec, bool streamable, bool lookback)
+{
+    if (T > kTile) return lookback ? Path::kLookback : Path::kCtaRowLoop;
+    if (T <= 32 * kItems) return Path::kWarpRows;
+    if (E == Est::kGae) return streamable ? Path::kWarpStream : Path::kWarpRows;
+    (void)N;
+    (void)vec;
+    return Path::kCtaRows;
+}
+
+// ------------------------------------------------------------------ CTA tile paths
 
 template <Est E, bool VEC, bool TRUNC>
-cudaError_t launch_variant(Params p, const LaunchShape &s, cudaStream_t stream)
+cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 {
-    p.rows_per_tile = s.rows_per_tile;
-    p.chunks_per_row = s.chunks_per_row;
-    p.segs = s.segs;
-    if (s.tiling == Tiling::kRows)
-        credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows>
-            <<<s.grid, kThreads, 0, stream>>>(p);
-    else if (s.tiling == Tiling::kRowLoop)
-        credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>
-            <<<s.grid, kThreads, 0, stream>>>(p);
-    else
-        credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback>
-            <<<s.grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (path == Path::kCtaRows) {
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = kTile / t_pad;
+        p.segs = 1;
+        const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows>,
+                          grid, kThreads, 0, stream, p);
+    }
+    p.chunks_per_row = kTile / kItems;
+    p.rows_per_tile = 1;
+    p.segs = (p.T + kTile - 1) / kTile;
+    if (path == Path::kLookback)
+        return launch_pdl(
+            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback>,
+            (unsigned)(p.N * p.segs), kThreads, 0, stream, p);
+    return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>,
+                      (unsigned)p.N, kThreads, 0, stream, p);
 }
 
-// Launch one estimator. With p.ws set (and T longer than a tile) the tiles of a row run
-// in parallel with decoupled look-back; otherwise a CTA walks each long row.
-template <Est E>
-cudaError_t launch_estimator(const Params &p, bool vec, cudaStream_t stream)
+// ------------------------------------------------------------------ warp paths
+
+template <Est E, bool VEC, bool TRUNC>
+cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 {
-    const LaunchShape s = plan_launch(p.N, p.T, p.ws != nullptr);
+    constexpr int CH = 32 * kItems;
+    int64_t jobs;
+    if (p.T <= CH) {
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.segs = 1;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = CH / t_pad;
+        jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
+    } else {
+        p.segs = (p.T + CH - 1) / CH;
+        p.chunks_per_row = CH / kItems;
+        p.rows_per_tile = 1;
+        jobs = p.N;
+    }
+    const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
+    return launch_pdl(credit_warp_kernel<E, kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+                      32 * kWarpsPerCta, 0, stream, p);
+}
+
+// Per-device grid limit (SMs x resident CTAs) of the warp-streaming kernel.
+constexpr int kMaxDevices = 64;
+template <Est E, bool TRUNC>
+struct WarpStreamConfig {
+    static std::atomic<int> grid_limit[kMaxDevices];
+};
+template <Est E, bool TRUNC>
+std::atomic<int> WarpStreamConfig<E, TRUNC>::grid_limit[kMaxDevices];
+
+template <Est E, bool TRUNC>
+cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
+{
+    auto kernel = credit_warp_stream_kernel<E, TRUNC, kWarpsPerCta>;
+    const int smem = kWarpsPerCta * warp_stages<E>() * WarpStage<E>::kBytes;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int limit = WarpStreamConfig<E, TRUNC>::grid_limit[dev].load(std::memory_order_relaxed);
+    if (limit == 0) {
+        int sms = 0, per_sm = 0;
+        if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem)) != cudaSuccess ||
+            (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess ||
+            (err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel,
+                                                                 32 * kWarpsPerCta, smem)) !=
+                cudaSuccess)
+            return err;
+        limit = sms * (per_sm > 0 ? per_sm : 1);
+        WarpStreamConfig<E, TRUNC>::grid_limit[dev].store(limit, std::memory_order_relaxed);
+    }
+    if (p.T <= kWarpChunk) {
+        p.segs = 1;
+        p.rows_per_tile = kWarpChunk / p.T;
+    } else {
+        p.segs = (p.T + kWarpChunk - 1) / kWarpChunk;
+        p.rows_per_tile = 1;
+    }
+    const int64_t units = p.segs == 1 ? (p.N + p.rows_per_tile - 1) / p.rows_per_tile : p.N;
+    const int64_t warps = (int64_t)limit * kWarpsPerCta;
+    const int64_t per_warp = (units + warps - 1) / warps;  // equal shares, one apart at most
+    const int64_t used = (units + per_warp - 1) / per_warp;
+    const unsigned grid = (unsigned)((used + kWarpsPerCta - 1) / kWarpsPerCta);
+    return launch_pdl(kernel, grid, 32 * kWarpsPerCta, smem, stream, p);
+}
+
+// ------------------------------------------------------------------ dispatch
+
+template <Est E, bool VEC, bool TRUNC>
+cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
+{
+    if (path == Path::kWarpRows) return launch_warp_rows<E, VEC, TRUNC>(p, stream);
+    return launch_cta<E, VEC, TRUNC>(p, path, stream);
+}
+
+// Launch one estimator; `vec` = 16-byte aligned rows (128-bit access), `streamable` =
+// layout fit for 16-byte bulk copies (see api.cu).
+template <Est E>
+cudaError_t launch_estimator(const Params &p, bool vec, bool streamable, cudaStream_t stream)
+{
+    const Path path = choose_path<E>(p.N, p.T, vec, streamable, p.ws != nullptr);
     const bool trunc = p.trunc != nullptr;
+    if (path == Path::kWarpStream)
+        return trunc ? launch_warp_stream<E, true>(p, stream)
+                     : launch_warp_stream<E, false>(p, stream);
     if (vec)
-        return trunc ? launch_variant<E, true, true>(p, s, stream)
-                     : launch_variant<E, true, false>(p, s, stream);
-    return trunc ? launch_variant<E, false, true>(p, s, stream)
-                 : launch_variant<E, false, false>(p, s, stream);
+        return trunc ? launch_path<E, true, true>(p, path, stream)
+                     : launch_path<E, true, false>(p, path, stream);
+    return trunc ? launch_path<E, false, true>(p, path, stream)
+                 : launch_path<E, false, false>(p, path, stream);
 }
 
 // One definition per estimator, each in its own translation unit.
-cudaError_t launch_return(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_td_lambda(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_gae(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_vtrace(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_retrace(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_return(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_gae(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_retrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
 
 }  // namespace rlca
