@@ -47,6 +47,7 @@ struct Params {
     float lambda;
     float gamma_lambda;        // gamma * lambda, rounded to fp32
     float gamma_one_m_lambda;  // gamma * (1 - lambda), rounded to fp32
+    float beta_pow;            // the constant beta to the power of the steps per thread
     float rho_bar;
     float c_bar;
     float pg_rho_bar;
@@ -70,6 +71,9 @@ struct EstTraits {
     static constexpr bool kNextAux = E == Est::kRetrace;
     static constexpr bool kNextRho = E == Est::kRetrace;
     static constexpr bool kTwoOutputs = E == Est::kGae || E == Est::kVtrace;
+    // beta_t is the same at every step that does not reset (gamma or gamma*lambda).
+    static constexpr bool kConstBeta =
+        E == Est::kReturn || E == Est::kTdLambda || E == Est::kGae;
 };
 
 // Raw inputs of one thread's ITEMS steps, plus the successor (step t0+ITEMS) of the
@@ -130,67 +134,75 @@ __device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next,
     return (j + 1 < ITEMS) ? a[j + 1] : next;
 }
 
-// alpha of one step given the value of the state after it (`nxt`).
-template <Est E>
-__device__ __forceinline__ float alpha_of(const Params &p, float r, float v, float rho_hat,
-                                          float nxt)
-{
-    if (E == Est::kReturn || E == Est::kTdLambda) return fmaf(p.gamma, nxt, r);
-    if (E == Est::kVtrace) return rho_hat * (fmaf(p.gamma, nxt, r) - v);
-    return fmaf(p.gamma, nxt, r) - v;  // GAE delta; Retrace with v = Q_t
-}
-
-// Forms (alpha, beta) of every item. V-trace keeps rho_t in c.x for the epilogue.
+// Forms (alpha, beta) of every item: one select picks the value of the state after the
+// step (the next step's value inside an episode, the successor value where it stops),
+// one picks beta or the reset marker. Successor values that need a load (truncated
+// steps and the window end) are fetched in a branch that few threads take.
+// V-trace keeps rho_t in c.x for the epilogue.
 template <Est E, int ITEMS>
 __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chunk<ITEMS> &c,
                                       Affine (&e)[ITEMS])
 {
-    float rho_hat[ITEMS];
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) c.sv[j] = 0.f;
+    // Steps whose successor value is loaded (Method section 3): truncated -> the supplied
+    // truncation value (read only there), window end -> the per-env bootstrap.
+    const unsigned load_sv = c.stop & c.valid & ~c.term;
+    if (load_sv) {
+        const int64_t off = row * p.ld;
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j)
+            if (load_sv & (1u << j))
+                c.sv[j] = (c.trunc & (1u << j)) ? __ldg(p.trunc_value + off + t0 + j)
+                                                : (p.boot ? __ldg(p.boot + row) : 0.f);
+    }
 #pragma unroll
     for (int j = 0; j < ITEMS; ++j) {
+        const bool stop = (c.stop >> j) & 1u;
         const float r = c.r[j];
-        rho_hat[j] = 1.f;
         if (E == Est::kReturn) {
-            e[j] = Affine{r, p.gamma};
+            e[j] = Affine{fmaf(p.gamma, c.sv[j], r), stop ? kResetB : p.gamma};
         } else if (E == Est::kTdLambda) {
-            e[j] = Affine{fmaf(p.gamma_one_m_lambda, at_or_next(c.v, c.v_next, j), r),
-                          p.gamma_lambda};
+            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
+            e[j] = Affine{fmaf(stop ? p.gamma : p.gamma_one_m_lambda, nxt, r),
+                          stop ? kResetB : p.gamma_lambda};
         } else if (E == Est::kGae) {
-            e[j] = Affine{alpha_of<E>(p, r, c.v[j], 0.f, at_or_next(c.v, c.v_next, j)),
-                          p.gamma_lambda};
+            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
+            e[j] = Affine{fmaf(p.gamma, nxt, r) - c.v[j], stop ? kResetB : p.gamma_lambda};
         } else if (E == Est::kVtrace) {
             const float rho = expf(c.x[j]);
             c.x[j] = rho;
-            rho_hat[j] = rho < p.rho_bar ? rho : p.rho_bar;
+            const float rho_hat = rho < p.rho_bar ? rho : p.rho_bar;
             const float cc = p.lambda * (rho < p.c_bar ? rho : p.c_bar);
-            e[j] = Affine{alpha_of<E>(p, r, c.v[j], rho_hat[j], at_or_next(c.v, c.v_next, j)),
-                          p.gamma * cc};
+            const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
+            e[j] = Affine{rho_hat * (fmaf(p.gamma, nxt, r) - c.v[j]), stop ? kResetB : p.gamma * cc};
         } else {  // Retrace: beta_t uses the trace of step t+1
             const float rho1 = at_or_next(c.y, c.y_next, j);
             const float c1 = p.lambda * (rho1 < 1.f ? rho1 : 1.f);
-            e[j] = Affine{alpha_of<E>(p, r, c.v[j], 0.f, at_or_next(c.x, c.x_next, j)),
-                          p.gamma * c1};
+            const float nxt = stop ? c.sv[j] : at_or_next(c.x, c.x_next, j);
+            e[j] = Affine{fmaf(p.gamma, nxt, r) - c.v[j], stop ? kResetB : p.gamma * c1};
         }
-        c.sv[j] = 0.f;
     }
-    if (c.stop) {
-        // Steps where the episode stops (Method section 3): successor value 0 if
-        // terminated, the truncation value if truncated (read only there), else the
-        // window-end bootstrap; the step resets. Padding items reset with value 0.
-        const int64_t off = row * p.ld;
+}
+
+// Composite of a thread's items, e_0 (+) e_1 (+) ... (+) e_{ITEMS-1}. With a constant
+// beta the composite beta is beta^ITEMS, or a reset if any item resets.
+template <Est E, int ITEMS>
+__device__ __forceinline__ Affine thread_aggregate(const Params &p, const Chunk<ITEMS> &c,
+                                                   const Affine (&e)[ITEMS])
+{
+    float a = e[ITEMS - 1].a;
 #pragma unroll
-        for (int j = 0; j < ITEMS; ++j) {
-            const unsigned bit = 1u << j;
-            if (c.stop & bit) {
-                float sv = 0.f;
-                if ((c.valid & bit) && !(c.term & bit))
-                    sv = (c.trunc & bit) ? __ldg(p.trunc_value + off + t0 + j)
-                                         : (p.boot ? __ldg(p.boot + row) : 0.f);
-                c.sv[j] = sv;
-                e[j] = Affine{alpha_of<E>(p, c.r[j], c.v[j], rho_hat[j], sv), kResetB};
-            }
-        }
+    for (int j = ITEMS - 2; j >= 0; --j) a = is_reset(e[j].b) ? e[j].a : fmaf(e[j].b, a, e[j].a);
+    float b;
+    if (EstTraits<E>::kConstBeta) {
+        b = c.stop ? kResetB : p.beta_pow;
+    } else {
+        b = e[ITEMS - 1].b;
+#pragma unroll
+        for (int j = ITEMS - 2; j >= 0; --j) b = is_reset(e[j].b) ? e[j].b : e[j].b * b;
     }
+    return Affine{a, b};
 }
 
 // Outputs of every item from A_t (A[j]) and A at the step after the chunk (a_after).

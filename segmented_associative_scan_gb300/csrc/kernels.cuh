@@ -157,9 +157,7 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
     build<E, ITEMS>(p, row, t0, c, e);
 
     // Thread aggregate: e_0 (+) e_1 (+) ... (+) e_{ITEMS-1}.
-    Affine agg = e[ITEMS - 1];
-#pragma unroll
-    for (int j = ITEMS - 2; j >= 0; --j) agg = affine_compose(e[j], agg);
+    const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
 
     // Warp suffix scan; the exclusive value of a lane is the inclusive one of lane+1.
     const Affine incl = warp_suffix_scan(agg, lane);
@@ -292,9 +290,7 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
     load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
     Affine e[ITEMS];
     build<E, ITEMS>(p, row, t0, c, e);
-    Affine agg = e[ITEMS - 1];
-#pragma unroll
-    for (int j = ITEMS - 2; j >= 0; --j) agg = affine_compose(e[j], agg);
+    const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
     const Affine incl = warp_suffix_scan(agg, lane);
     Affine excl = shfl_down(incl, 1);
     if (lane == 31) excl = affine_identity();

@@ -182,8 +182,14 @@ cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
 // Launch one estimator; `vec` = 16-byte aligned rows (128-bit access), `streamable` =
 // layout fit for 16-byte bulk copies (see api.cu).
 template <Est E>
-cudaError_t launch_estimator(const Params &p, bool vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_estimator(const Params &p_in, bool vec, bool streamable, cudaStream_t stream)
 {
+    Params p = p_in;
+    // beta^kItems in the order the kernels multiply (b = beta * b), for the constant-beta
+    // estimators' per-thread composite.
+    const float beta = E == Est::kReturn ? p.gamma : p.gamma_lambda;
+    p.beta_pow = beta;
+    for (int i = 1; i < kItems; ++i) p.beta_pow = beta * p.beta_pow;
     const Path path = choose_path<E>(p.N, p.T, vec, streamable, p.ws != nullptr);
     const bool trunc = p.trunc != nullptr;
     if (path == Path::kWarpStream)

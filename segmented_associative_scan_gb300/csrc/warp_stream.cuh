@@ -135,9 +135,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_stream_kernel(const Pa
 
         Affine e[ITEMS];
         build<E, ITEMS>(p, row, t0, c, e);
-        Affine agg = e[ITEMS - 1];
-#pragma unroll
-        for (int i = ITEMS - 2; i >= 0; --i) agg = affine_compose(e[i], agg);
+        const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
         const Affine incl = warp_suffix_scan(agg, lane);
         Affine excl = shfl_down(incl, 1);
         if (lane == 31) excl = affine_identity();
