@@ -161,14 +161,13 @@ __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chun
         const bool stop = (c.stop >> j) & 1u;
         const float r = c.r[j];
         if (E == Est::kReturn) {
-            e[j] = Affine{fmaf(p.gamma, c.sv[j], r), stop ? kResetB : p.gamma};
+            e[j] = Affine{fmaf(p.gamma, c.sv[j], r), 0.f};  // beta: const_beta + stop bit
         } else if (E == Est::kTdLambda) {
             const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
-            e[j] = Affine{fmaf(stop ? p.gamma : p.gamma_one_m_lambda, nxt, r),
-                          stop ? kResetB : p.gamma_lambda};
+            e[j] = Affine{fmaf(stop ? p.gamma : p.gamma_one_m_lambda, nxt, r), 0.f};
         } else if (E == Est::kGae) {
             const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
-            e[j] = Affine{fmaf(p.gamma, nxt, r) - c.v[j], stop ? kResetB : p.gamma_lambda};
+            e[j] = Affine{fmaf(p.gamma, nxt, r) - c.v[j], 0.f};
         } else if (E == Est::kVtrace) {
             const float rho = expf(c.x[j]);
             c.x[j] = rho;
@@ -185,6 +184,24 @@ __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chun
     }
 }
 
+// The constant beta of the constant-beta estimators.
+template <Est E>
+__device__ __forceinline__ float const_beta(const Params &p)
+{
+    return E == Est::kReturn ? p.gamma : p.gamma_lambda;
+}
+
+// A at item j from A at item j+1 (x). With a constant beta the reset test reads the stop
+// bit and the multiplier is the scalar beta, so per-item betas are never formed.
+template <Est E, int ITEMS>
+__device__ __forceinline__ float step_apply(const Params &p, const Chunk<ITEMS> &c,
+                                            const Affine (&e)[ITEMS], int j, float x)
+{
+    if (EstTraits<E>::kConstBeta)
+        return ((c.stop >> j) & 1u) ? e[j].a : fmaf(const_beta<E>(p), x, e[j].a);
+    return affine_apply(e[j], x);
+}
+
 // Composite of a thread's items, e_0 (+) e_1 (+) ... (+) e_{ITEMS-1}. With a constant
 // beta the composite beta is beta^ITEMS, or a reset if any item resets.
 template <Est E, int ITEMS>
@@ -193,7 +210,7 @@ __device__ __forceinline__ Affine thread_aggregate(const Params &p, const Chunk<
 {
     float a = e[ITEMS - 1].a;
 #pragma unroll
-    for (int j = ITEMS - 2; j >= 0; --j) a = is_reset(e[j].b) ? e[j].a : fmaf(e[j].b, a, e[j].a);
+    for (int j = ITEMS - 2; j >= 0; --j) a = step_apply<E, ITEMS>(p, c, e, j, a);
     float b;
     if (EstTraits<E>::kConstBeta) {
         b = c.stop ? kResetB : p.beta_pow;
@@ -203,6 +220,16 @@ __device__ __forceinline__ Affine thread_aggregate(const Params &p, const Chunk<
         for (int j = ITEMS - 2; j >= 0; --j) b = is_reset(e[j].b) ? e[j].b : e[j].b * b;
     }
     return Affine{a, b};
+}
+
+// Every A_t of the thread's items from A after the last item (a_after).
+template <Est E, int ITEMS>
+__device__ __forceinline__ void replay(const Params &p, const Chunk<ITEMS> &c,
+                                       const Affine (&e)[ITEMS], float a_after, float (&A)[ITEMS])
+{
+    A[ITEMS - 1] = step_apply<E, ITEMS>(p, c, e, ITEMS - 1, a_after);
+#pragma unroll
+    for (int j = ITEMS - 2; j >= 0; --j) A[j] = step_apply<E, ITEMS>(p, c, e, j, A[j + 1]);
 }
 
 // Outputs of every item from A_t (A[j]) and A at the step after the chunk (a_after).

@@ -200,9 +200,7 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
     const float tile_first = affine_apply(whole, carry_in);
 
     float A[ITEMS];
-    A[ITEMS - 1] = affine_apply(e[ITEMS - 1], a_after);
-#pragma unroll
-    for (int j = ITEMS - 2; j >= 0; --j) A[j] = affine_apply(e[j], A[j + 1]);
+    replay<E, ITEMS>(p, c, e, a_after, A);
     epilogue<E, ITEMS, VEC>(p, c, A, a_after, row, t0);
     return tile_first;
 }
@@ -297,9 +295,7 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
     const Affine whole = shfl_idx(incl, 0);
     const float a_after = affine_apply(excl, carry_in);
     float A[ITEMS];
-    A[ITEMS - 1] = affine_apply(e[ITEMS - 1], a_after);
-#pragma unroll
-    for (int j = ITEMS - 2; j >= 0; --j) A[j] = affine_apply(e[j], A[j + 1]);
+    replay<E, ITEMS>(p, c, e, a_after, A);
     epilogue<E, ITEMS, VEC>(p, c, A, a_after, row, t0);
     return affine_apply(whole, carry_in);
 }

@@ -142,9 +142,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_stream_kernel(const Pa
         const Affine whole = shfl_idx(incl, 0);
         const float a_after = affine_apply(excl, carry_in);
         float A[ITEMS];
-        A[ITEMS - 1] = affine_apply(e[ITEMS - 1], a_after);
-#pragma unroll
-        for (int i = ITEMS - 2; i >= 0; --i) A[i] = affine_apply(e[i], A[i + 1]);
+        replay<E, ITEMS>(p, c, e, a_after, A);
         epilogue<E, ITEMS, true>(p, c, A, a_after, row, t0);
         carry = affine_apply(whole, carry_in);
         warp_advance(p, cons);
