@@ -36,15 +36,29 @@ METRIC = "credit-assignment timesteps/sec at [4096,1024] fp32; % of GB300 HBM ro
 UNIT = "timesteps/s"
 N_ENVS, SEQ_LEN = 4096, 1024
 WORKLOAD = "GAE with truncation bootstrapping, fp32, num_envs=4096, seq_len=1024"
+WORKLOADS = {
+    "gae": WORKLOAD,
+    "return": "discounted return, fp32, num_envs=4096, seq_len=1024 (rates of the [4096,128] return/TD workload)",
+    "td_lambda": "TD(lambda=0.9), fp32, num_envs=4096, seq_len=1024 (rates of the [4096,128] return/TD workload)",
+    "vtrace": "V-trace, fp32, num_envs=4096, seq_len=1024 (rates of the [8192,256] V-trace workload)",
+    "retrace": "Retrace, fp32, num_envs=4096, seq_len=1024 (rates of the [2048,4096] Retrace workload)",
+}
+KERNELS = {
+    "gae": "credit_warp_stream_kernel<GAE> (warp-owned rows, per-warp TMA ring)",
+    "return": "credit_scan_kernel<return, whole-row CTA tiles>",
+    "td_lambda": "credit_scan_kernel<TD(lambda), whole-row CTA tiles>",
+    "vtrace": "credit_scan_kernel<V-trace, whole-row CTA tiles>",
+    "retrace": "credit_scan_kernel<Retrace, whole-row CTA tiles>",
+}
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes per launch measured by ncu for the GAE [4096,1024] kernel, keyed by a hash of
 # the kernel sources at the time of the capture; null once the kernels change.
 NCU_TRAFFIC = {
-    # credit_warp_stream_kernel<GAE>: dram read 43.01 MB + write 0.98 MB in one captured
-    # launch (outputs stay in L2 within it): profiles/gae_trunc_4096x1024_warp_stream_kernel.md
-    "2e33c7daeb6c28e1": 43_991_552,
+    # credit_warp_stream_kernel<GAE>: dram read 43.01 MB + write 1.13 MB in one captured
+    # launch (the outputs stay in L2 within it): profiles/gae_trunc_4096x1024_kernel.md
+    "152a3feb6fd0aaad": 44_138_240,
 }
 
 
@@ -258,7 +272,9 @@ def timed_replay(torch, graphs):
 
 
 def n_sets_for(bytes_per_set):
-    return max(3, int(np.ceil(2.5 * L2_BYTES / bytes_per_set)))
+    """Input sets to rotate so that their total exceeds the L2 cache 2.5 times (at most
+    64 sets; tiny problems then stay L2-resident, which the config line states)."""
+    return min(64, max(3, int(np.ceil(2.5 * L2_BYTES / bytes_per_set))))
 
 
 def per_estimator_roofline(torch, rlca, device, peak):
@@ -356,23 +372,25 @@ def gpu_arm(args, rank, world, local_rank, dist):
     peak, peak_src = measured_peaks()
 
     # Distinct seeded batches, resident in HBM, rotating so their total exceeds L2.
-    ro0 = workload_inputs("gae", N_ENVS, SEQ_LEN, seed=1000 * rank)
-    nbytes = algorithmic_bytes("gae", ro0)
+    est = args.estimator
+    N, T = args.num_envs, args.seq_len
+    ro0 = workload_inputs(est, N, T, seed=1000 * rank)
+    nbytes = algorithmic_bytes(est, ro0)
     n_sets = n_sets_for(nbytes)
     sets = [DeviceSet(ro0, device)]
     for i in range(1, n_sets):
-        sets.append(DeviceSet(workload_inputs("gae", N_ENVS, SEQ_LEN, 1000 * rank + i), device))
-    params = est_params("gae", ro0)
-    step_bytes = [algorithmic_bytes("gae", s.ro) for s in sets]
+        sets.append(DeviceSet(workload_inputs(est, N, T, 1000 * rank + i), device))
+    params = est_params(est, ro0)
+    step_bytes = [algorithmic_bytes(est, s.ro) for s in sets]
 
     K, W = args.steps, args.warmup
     for i in range(W):
-        launch(rlca, "gae", sets[i % n_sets], params)
+        launch(rlca, est, sets[i % n_sets], params)
     torch.cuda.synchronize()
     G = n_sets * max(1, 96 // n_sets)
-    graphs = [capture(torch, rlca, "gae", sets, params, G)] * (K // G)
+    graphs = [capture(torch, rlca, est, sets, params, G)] * (K // G)
     if K % G:
-        graphs.append(capture(torch, rlca, "gae", sets, params, K % G))
+        graphs.append(capture(torch, rlca, est, sets, params, K % G))
     graphs[0].replay()
     torch.cuda.synchronize()
     kernel_bytes_per_step = sum(step_bytes[i % n_sets] for i in range(K)) / K
@@ -402,7 +420,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
 
     launch_us = 1000.0 * ms / K
     achieved = kernel_bytes_per_step / (launch_us * 1e-6) / 1e9
-    value = job_throughput(world, N_ENVS, SEQ_LEN, K, ms_max)
+    value = job_throughput(world, N, T, K, ms_max)
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(src_hash)
     result = {
@@ -411,32 +429,34 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded rollouts with the workload's distributions (no dataset)",
         "config": {
-            "workload": WORKLOAD, "estimator": "gae", "num_envs": N_ENVS,
-            "seq_len": SEQ_LEN, "gamma": params["gamma"], "lambda": params["lam"],
+            "workload": WORKLOADS[est] if (N, T) == (N_ENVS, SEQ_LEN)
+            else f"{est}, fp32, num_envs={N}, seq_len={T}", "estimator": est, "num_envs": N,
+            "seq_len": T, "gamma": params["gamma"], "lambda": params.get("lam"),
             "input_sets": n_sets,
-            "l2": f"inputs larger than L2: {n_sets} distinct batches of "
-                  f"{nbytes / 1e6:.1f} MB rotate ({n_sets * nbytes / 1e6:.0f} MB > "
-                  f"{L2_BYTES / 1e6:.0f} MB L2)",
+            "l2": (f"inputs larger than L2: {n_sets} distinct batches of "
+                   f"{nbytes / 1e6:.1f} MB rotate ({n_sets * nbytes / 1e6:.0f} MB > "
+                   f"{L2_BYTES / 1e6:.0f} MB L2)") if n_sets * nbytes > L2_BYTES else
+                  (f"{n_sets} batches of {nbytes / 1e6:.2f} MB rotate; they fit in L2"),
             "timing": f"CUDA graphs of {G} launches replayed between CUDA events on the "
                       "launch stream; one fused kernel launch per step",
             "parallelism": f"replicas{world}: each GPU its own batch, no collective"},
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": "credit_warp_stream_kernel<GAE> (warp-owned rows, per-warp TMA ring)",
+            "kernel": KERNELS[est],
             "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),
             "launch_us": round(launch_us, 3), "peak_source": peak_src,
             "frac_of_8tbs": round(achieved / 8000.0, 4), "kernel_source": src_hash},
         "gpu_launches": K,
         "clocks": clocks,
     }
-    if not args.no_e2e:
+    if not args.no_e2e and est == "gae":
         result["e2e"] = e2e_run(torch, rlca, ro0, device, min(K, args.e2e_steps))
     del graphs, sets
     torch.cuda.empty_cache()
-    if world == 1 and not args.no_estimators:
+    if world == 1 and not args.no_estimators and (N, T) == (N_ENVS, SEQ_LEN):
         result["estimators"] = per_estimator_roofline(torch, rlca, device, peak)
-    if world == 1 and args.cpu_seconds > 0:
+    if world == 1 and args.cpu_seconds > 0 and est == "gae":
         result["cpu_baseline"] = cpu_baseline(ro0, args.cpu_seconds)
     return result
 
@@ -491,6 +511,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("rlca", "reference"), default="rlca")
+    ap.add_argument("--num-envs", type=int, default=N_ENVS)
+    ap.add_argument("--seq-len", type=int, default=SEQ_LEN)
+    ap.add_argument("--estimator", choices=tuple(WORKLOADS), default="gae",
+                    help="estimator timed in the main loop (the metric's workload is gae)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
