@@ -10,7 +10,10 @@ Assignment", Method section 3 (termination: successor value 0; truncation: suppl
 bootstrap value; window end t = T-1: per-env bootstrap, counted once). The formulas are
 spelled out in ``rlca_oracle.c``.
 
-Parity pins (tests/test_oracle_pins.py): closed-form returns, hand-computed golden
+Also the forward-time scans: eligibility traces and episodic prefix sums.
+
+Parity pins (tests/test_oracle_pins.py, tests/test_oracle_forward_pins.py): closed-form
+returns and traces, hand-computed golden
 examples, GAE(lambda=1) = return - V, GAE(lambda=0) = TD error, TD(lambda) = GAE returns,
 non-recursive sum definitions (GAE, lambda-return as weighted n-step returns, IMPALA
 V-trace sum, Retrace sum), on-policy reductions of V-trace and Retrace, and per-episode
@@ -55,6 +58,8 @@ _SIGS = {
     "oracle_td_lambda": [_F, _F, _F, _F, _F, _F, _D, _D, _I, _I, _I, _F],
     "oracle_vtrace": [_F, _F, _F, _F, _F, _F, _F, _D, _D, _D, _D, _D, _I, _I, _I, _F, _F],
     "oracle_retrace": [_F, _F, _F, _F, _F, _F, _F, _F, _D, _D, _I, _I, _I, _F],
+    "oracle_eligibility_trace": [_F, _F, _F, _F, _D, _I, _I, _I, _F],
+    "oracle_episodic_prefix_sum": [_F, _F, _F, _F, _I, _I, _I, _F],
 }
 
 
@@ -161,4 +166,35 @@ def retrace(reward, q_taken, expected_q, rho, terminated, truncated=None, trunc_
     out = np.empty((N, T), np.float64)
     _load().oracle_retrace(r, q, e, p, d, tr, tv, b, _f32(gamma), _f32(lam), N, T, ld,
                            out.ctypes.data)
+    return out
+
+
+def _forward_args(x, terminated, truncated, init):
+    keep = []
+    ptrs = []
+    for a, dt in ((x, np.float32), (terminated, np.uint8), (truncated, np.uint8),
+                  (init, np.float32)):
+        arr, ptr = _p(a, dt)
+        keep.append(arr)
+        ptrs.append(ptr)
+    return keep, ptrs
+
+
+def eligibility_trace(x, terminated, truncated=None, init=None, decay=0.95, T=None):
+    """Forward accumulating trace e_t = x_t + decay * e_{t-1}, fresh after an episode end,
+    e_{-1} = init (rl-triton technical summary, Method section 1: the forward-time mirror
+    of the recurrence)."""
+    N, T, ld = _shape(x, T)
+    keep, (xp, d, tr, ini) = _forward_args(x, terminated, truncated, init)
+    out = np.empty((N, T), np.float64)
+    _load().oracle_eligibility_trace(xp, d, tr, ini, _f32(decay), N, T, ld, out.ctypes.data)
+    return out
+
+
+def episodic_prefix_sum(x, terminated, truncated=None, init=None, T=None):
+    """Forward sum within each episode (Method section 1: episodic prefix sums)."""
+    N, T, ld = _shape(x, T)
+    keep, (xp, d, tr, ini) = _forward_args(x, terminated, truncated, init)
+    out = np.empty((N, T), np.float64)
+    _load().oracle_episodic_prefix_sum(xp, d, tr, ini, N, T, ld, out.ctypes.data)
     return out

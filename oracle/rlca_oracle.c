@@ -181,3 +181,45 @@ void oracle_retrace(const float *reward, const float *q_taken, const float *expe
         }
     }
 }
+
+/* ------------------------------------------------------------------ forward scans
+ * The forward-time mirror of the recurrence (Method section 1: eligibility traces run
+ * the same first-order recurrence forward in time; episodic prefix sums are its decay-1
+ * case): A_t = x_t + decay * A_{t-1} inside an episode. A step that follows the end of
+ * an episode (the previous step terminated or truncated) starts afresh: A_t = x_t. At
+ * the window start A_{-1} is the per-env carried-in value init[n] (NULL means 0), the
+ * forward counterpart of the window-end bootstrap (Method section 3). */
+
+/* Accumulating eligibility trace e_t = x_t + decay * e_{t-1} (decay = gamma * lambda). */
+void oracle_eligibility_trace(const float *x, const uint8_t *term, const uint8_t *trunc,
+                              const float *init, double decay, int64_t N, int64_t T,
+                              int64_t ld, double *trace)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double prev = init ? (double)init[n] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t i = n * ld + t;
+            int fresh = t > 0 && (term[i - 1] || (trunc && trunc[i - 1]));
+            double e = fresh ? (double)x[i] : (double)x[i] + decay * prev;
+            trace[n * T + t] = e;
+            prev = e;
+        }
+    }
+}
+
+/* Episodic prefix sum S_t = x_t + S_{t-1} inside an episode. */
+void oracle_episodic_prefix_sum(const float *x, const uint8_t *term, const uint8_t *trunc,
+                                const float *init, int64_t N, int64_t T, int64_t ld,
+                                double *sum)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double prev = init ? (double)init[n] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t i = n * ld + t;
+            int fresh = t > 0 && (term[i - 1] || (trunc && trunc[i - 1]));
+            double s = fresh ? (double)x[i] : (double)x[i] + prev;
+            sum[n * T + t] = s;
+            prev = s;
+        }
+    }
+}
