@@ -143,6 +143,27 @@ int rlca_retrace(const float *reward, const float *q_taken, const float *expecte
                  void *stream);
 
 /*
+ * Forward-time scans (Method section 1: eligibility traces are the forward-time mirror
+ * of the recurrence; episodic prefix sums are among the estimators it covers).
+ *   A_t = x_t + decay * A_{t-1} inside an episode; A_t = x_t at a step whose previous
+ *   step terminated or truncated (a new episode); A_{-1} = init[n] at the window start
+ *   (nullable = 0), the value carried in from the previous window.
+ * Inputs: x, terminated [N,ld]; truncated [N,ld] (nullable; no values needed: a
+ * truncation only ends the episode here); init [N] (nullable). Output [N,ld].
+ * Errors as above; decay must be finite and >= 0 (RLCA_ERR_PARAM otherwise).
+ */
+
+/* Accumulating eligibility trace e_t = x_t + decay * e_{t-1} (decay = gamma * lambda). */
+int rlca_eligibility_trace(const float *x, const uint8_t *terminated,
+                           const uint8_t *truncated, const float *init, float decay, int64_t N,
+                           int64_t T, int64_t ld, float *traces, void *stream);
+
+/* Episodic prefix sum S_t = x_t + S_{t-1} (decay 1). */
+int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
+                             const uint8_t *truncated, const float *init, int64_t N, int64_t T,
+                             int64_t ld, float *sums, void *stream);
+
+/*
  * Long sequences: tiles scanned in parallel with decoupled look-back.
  *
  * The kernels scan tiles of 1024 steps. When T > 1024 a row spans several tiles. The

@@ -39,6 +39,8 @@ SIGNATURES = {
                      _P, _P], ctypes.c_int),
     "rlca_retrace": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P],
                      ctypes.c_int),
+    "rlca_eligibility_trace": ([_P, _P, _P, _P, _F, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+    "rlca_episodic_prefix_sum": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "rlca_workspace_bytes": ([_I64, _I64], ctypes.c_size_t),
     "rlca_workspace_check": ([_P, _P], ctypes.c_int),
     "rlca_testing_lookback_stall": ([_P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, ctypes.c_int,
@@ -251,9 +253,35 @@ def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
     return q_ret
 
 
+def rlca_eligibility_trace(x, terminated, truncated=None, init=None, decay=0.95,
+                           traces=None):
+    """Forward accumulating trace e_t = x_t + decay e_{t-1}, fresh after an episode ends,
+    e_{-1} = init."""
+    g = _Rows(x)
+    args = (g.ptr(x, "x", _F32), g.ptr(terminated, "terminated", _FLAG),
+            g.ptr(truncated, "truncated", _FLAG, True), g.vec_ptr(init, "init"))
+    traces = g.out(traces, "traces")
+    _check("rlca_eligibility_trace", lib().rlca_eligibility_trace(
+        *args, decay, g.N, g.T, g.ld, traces.data_ptr() or None, _stream(g.device)))
+    return traces
+
+
+def rlca_episodic_prefix_sum(x, terminated, truncated=None, init=None, sums=None):
+    """Forward sum of x within each episode, S_{-1} = init."""
+    g = _Rows(x)
+    args = (g.ptr(x, "x", _F32), g.ptr(terminated, "terminated", _FLAG),
+            g.ptr(truncated, "truncated", _FLAG, True), g.vec_ptr(init, "init"))
+    sums = g.out(sums, "sums")
+    _check("rlca_episodic_prefix_sum", lib().rlca_episodic_prefix_sum(
+        *args, g.N, g.T, g.ld, sums.data_ptr() or None, _stream(g.device)))
+    return sums
+
+
 # Short names.
 discounted_return = rlca_discounted_return
 td_lambda = rlca_td_lambda
 gae = rlca_gae
 vtrace = rlca_vtrace
 retrace = rlca_retrace
+eligibility_trace = rlca_eligibility_trace
+episodic_prefix_sum = rlca_episodic_prefix_sum

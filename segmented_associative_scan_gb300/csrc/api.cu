@@ -60,17 +60,15 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
     for (int i = 0; i < n_in; ++i)
         if (!f32_in[i]) return RLCA_ERR_NULL;
     if (!p.term || !outs[0]) return RLCA_ERR_NULL;
-    if (p.trunc && !p.trunc_value) return RLCA_ERR_NULL;
+    if (p.trunc && !p.trunc_value && !p.forward) return RLCA_ERR_NULL;
 
     // Outputs may overlap neither an input nor each other.
     Range in_ranges[8];
     int k = 0;
     for (int i = 0; i < n_in; ++i) in_ranges[k++] = span(f32_in[i], p.N, p.T, p.ld, 4);
     in_ranges[k++] = span(p.term, p.N, p.T, p.ld, 1);
-    if (p.trunc) {
-        in_ranges[k++] = span(p.trunc, p.N, p.T, p.ld, 1);
-        in_ranges[k++] = span(p.trunc_value, p.N, p.T, p.ld, 4);
-    }
+    if (p.trunc) in_ranges[k++] = span(p.trunc, p.N, p.T, p.ld, 1);
+    if (p.trunc_value) in_ranges[k++] = span(p.trunc_value, p.N, p.T, p.ld, 4);
     if (p.boot) in_ranges[k++] = span(p.boot, 1, p.N, p.N, 4);
     for (int o = 0; o < n_out; ++o) {
         if (!outs[o]) continue;
@@ -220,6 +218,25 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
 }
 
+// Forward scans: x and flags as the reverse estimators' reward and flags; `init` is the
+// per-env value carried into the window (nullable); decay >= 0 and finite.
+int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *truncated,
+                 const float *init, float decay, int64_t N, int64_t T, int64_t ld, float *out,
+                 void *stream)
+{
+    if (!std::isfinite(decay) || decay < 0.f) return RLCA_ERR_PARAM;
+    Params p = base_params(x, terminated, truncated, nullptr, init, decay, 1.f, N, T, ld);
+    p.trunc = truncated;  // truncation needs no successor values here
+    p.forward = 1;
+    p.out0 = out;
+    const float *in[] = {x};
+    float *outs[] = {out};
+    auto launch = [](const Params &q, bool vec, bool, cudaStream_t s) {
+        return rlca::launch_forward(q, vec, s);
+    };
+    return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream);
+}
+
 constexpr Workspace kNoWorkspace{nullptr, 0};
 
 }  // namespace
@@ -366,6 +383,20 @@ int rlca_retrace_ex(const float *reward, const float *q_taken, const float *expe
     return retrace(reward, q_taken, expected_q, rho, terminated, truncated, trunc_value,
                    bootstrap_ev, gamma, lambda, N, T, ld, q_ret,
                    Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_eligibility_trace(const float *x, const uint8_t *terminated,
+                           const uint8_t *truncated, const float *init, float decay, int64_t N,
+                           int64_t T, int64_t ld, float *traces, void *stream)
+{
+    return forward_scan(x, terminated, truncated, init, decay, N, T, ld, traces, stream);
+}
+
+int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
+                             const uint8_t *truncated, const float *init, int64_t N, int64_t T,
+                             int64_t ld, float *sums, void *stream)
+{
+    return forward_scan(x, terminated, truncated, init, 1.f, N, T, ld, sums, stream);
 }
 
 int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, int64_t N,

@@ -1,0 +1,44 @@
+// Forward scans (eligibility traces, episodic prefix sums) in a translation unit of
+// their own: warp-owned rows, walked from the first step to the last.
+#include "forward.cuh"
+#include "launch.cuh"
+
+namespace rlca {
+
+template <bool VEC, bool TRUNC>
+cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
+{
+    constexpr int CH = 32 * kItems;
+    int64_t jobs;
+    if (p.T <= CH) {
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.segs = 1;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = CH / t_pad;
+        jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
+    } else {
+        p.segs = (p.T + CH - 1) / CH;
+        p.chunks_per_row = CH / kItems;
+        p.rows_per_tile = 1;
+        jobs = p.N;
+    }
+    const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
+    return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+                      32 * kWarpsPerCta, 0, stream, p);
+}
+
+cudaError_t launch_forward(const Params &p_in, bool vec, cudaStream_t stream)
+{
+    Params p = p_in;
+    // decay^kItems in the kernel's multiply order, for the per-lane composite.
+    p.beta_pow = p.gamma;
+    for (int i = 1; i < kItems; ++i) p.beta_pow = p.gamma * p.beta_pow;
+    const bool trunc = p.trunc != nullptr;
+    if (vec)
+        return trunc ? launch_forward_variant<true, true>(p, stream)
+                     : launch_forward_variant<true, false>(p, stream);
+    return trunc ? launch_forward_variant<false, true>(p, stream)
+                 : launch_forward_variant<false, false>(p, stream);
+}
+
+}  // namespace rlca

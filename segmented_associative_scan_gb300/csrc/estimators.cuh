@@ -59,6 +59,7 @@ struct Params {
     void *ws;         // caller-owned workspace: header + one 32-byte state per tile
     int spin_limit;   // consecutive empty polls of a later tile before giving up
     int stall;        // testing only: nonzero = tiles never publish their state
+    int forward;      // host-side only: a forward scan (truncation needs no values)
 };
 
 template <Est E>

@@ -1,0 +1,109 @@
+// Forward-time scans: eligibility traces and episodic prefix sums.
+//
+// Method section 1 of "rl-triton: High-Performance Triton GPU Kernels for Reinforcement
+// Learning Credit Assignment" lists eligibility traces (the forward-time mirror of the
+// recurrence) and episodic prefix sums among the estimators. Both are
+//   A_t = x_t + decay * A_{t-1}   inside an episode,   A_t = x_t   right after one ends,
+// with A_{-1} = init[n] carried into the window (the forward counterpart of the window-end
+// bootstrap of Method section 3); prefix sums have decay = 1. The same operator composes
+// them, applied in the other time order: a warp prefix scan (shfl_up) instead of a
+// suffix scan, chunks walked from the first to the last.
+//
+// Every warp owns whole rows, as in the warp-owned reverse kernel: several short rows
+// per warp (each row's first step resets and folds in init), or one long row walked in
+// chunks of 32 * ITEMS steps with the carry in a register. No CTA barrier, no shared
+// memory. decay >= 0 (checked on the host), so the reset marker of the scan is exact.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace rlca {
+
+// One chunk: A at the step before the chunk is `carry_in`; `prev_ended` says whether the
+// step before lane 0's first step ended an episode. Returns A at the chunk's last step;
+// *last_ended gets whether that step ended an episode.
+template <int ITEMS, bool VEC, bool TRUNC>
+__device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int t0, bool active,
+                                               float carry_in, bool prev_ended,
+                                               bool *last_ended)
+{
+    const int lane = threadIdx.x & 31;
+    const int T = p.T;
+    const int Te = active ? T : 0;
+    const int64_t off = active ? row * p.ld : 0;
+
+    float x[ITEMS];
+    load_items<ITEMS, VEC>(p.reward + off, t0, Te, x);
+    unsigned ended = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
+    if (TRUNC) ended |= load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te);
+    const unsigned valid = valid_items<ITEMS>(t0, Te);
+
+    // Item j starts afresh when step t0+j-1 ended an episode; the row's first step resets
+    // too and takes the carried-in value as its own term.
+    const unsigned prev_lane = __shfl_up_sync(kFullMask, ended >> (ITEMS - 1), 1) & 1u;
+    const unsigned before = lane == 0 ? (prev_ended ? 1u : 0u) : prev_lane;
+    unsigned reset = ((ended << 1) | before) | ~valid;
+    if (t0 == 0 && active) {
+        reset |= 1u;
+        if (p.boot) x[0] = fmaf(p.gamma, __ldg(p.boot + row), x[0]);
+    }
+    reset &= all_items<ITEMS>();
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j)
+        if (!((valid >> j) & 1u)) x[j] = 0.f;
+
+    // Composite of the lane's items in time order, e_{ITEMS-1} o ... o e_0.
+    const float decay = p.gamma;
+    float a = x[0];
+#pragma unroll
+    for (int j = 1; j < ITEMS; ++j) a = ((reset >> j) & 1u) ? x[j] : fmaf(decay, a, x[j]);
+    const Affine agg{a, reset ? kResetB : p.beta_pow};
+
+    // Inclusive prefix scan over lanes: lane i gets agg_i o ... o agg_0.
+    Affine incl = agg;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Affine y{__shfl_up_sync(kFullMask, incl.a, d), __shfl_up_sync(kFullMask, incl.b, d)};
+        if (lane >= d) incl = affine_compose(incl, y);
+    }
+    Affine excl{__shfl_up_sync(kFullMask, incl.a, 1), __shfl_up_sync(kFullMask, incl.b, 1)};
+    if (lane == 0) excl = affine_identity();
+    const Affine whole = shfl_idx(incl, 31);
+
+    float A[ITEMS];
+    float prev = affine_apply(excl, carry_in);
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        prev = ((reset >> j) & 1u) ? x[j] : fmaf(decay, prev, x[j]);
+        A[j] = prev;
+    }
+    if (valid) store_items<ITEMS, VEC>(p.out0 + off, t0, valid, A);
+    *last_ended = (__shfl_sync(kFullMask, ended, 31) >> (ITEMS - 1)) & 1u;
+    return affine_apply(whole, carry_in);
+}
+
+template <int ITEMS, bool VEC, bool TRUNC, int WARPS = 4>
+__global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params p)
+{
+    grid_dependency_sync();
+    constexpr int CH = 32 * ITEMS;
+    const int lane = threadIdx.x & 31;
+    const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    bool last_ended = false;
+    if (p.segs == 1) {
+        const int local_row = lane / p.chunks_per_row;
+        const int chunk = lane - local_row * p.chunks_per_row;
+        const int64_t row = job * p.rows_per_tile + local_row;
+        const bool active = local_row < p.rows_per_tile && row < p.N;
+        forward_chunk<ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f, false,
+                                         &last_ended);
+    } else {
+        if (job >= p.N) return;  // the whole warp leaves together
+        float carry = 0.f;
+        for (int s = 0; s < p.segs; ++s)
+            carry = forward_chunk<ITEMS, VEC, TRUNC>(p, job, s * CH + lane * ITEMS, true,
+                                                     carry, last_ended, &last_ended);
+    }
+}
+
+}  // namespace rlca

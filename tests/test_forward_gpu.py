@@ -1,0 +1,121 @@
+"""GPU parity of the forward scans (eligibility traces, episodic prefix sums) against
+the fp64 oracle: shape grid with ragged tails and several rows per warp, flag patterns,
+strided and unaligned layouts with guard zones, and exact NaN isolation."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import segmented_associative_scan_gb300 as rlca
+import synthetic_rollouts as sr
+from parity_helpers import SENTINEL, TOL, Placed, assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device(cuda_device):
+    rlca.build()
+    rlca.lib()
+
+
+def run_both(ro, kind, decay=0.95, ld=None, offset=0, with_trunc=True, with_init=True):
+    N, T = ro.N, ro.T
+    ld = T if ld is None else ld
+    dev = "cuda:0"
+    x = Placed(ro.value, N, T, ld, offset, torch.float32, 0.0, dev)
+    d = Placed(ro.terminated, N, T, ld, offset, torch.uint8, 1, dev)
+    tr = Placed(ro.truncated, N, T, ld, offset, torch.uint8, 1, dev) if with_trunc else None
+    init = torch.from_numpy(ro.bootstrap).to(dev) if with_init else None
+    out = Placed(None, N, T, ld, offset, torch.float32, SENTINEL, dev)
+    trn = tr.view if tr is not None else None
+    if kind == "trace":
+        rlca.rlca_eligibility_trace(x.view, d.view, trn, init, decay=decay, traces=out.view)
+        ref = oracle.eligibility_trace(ro.value, ro.terminated,
+                                       ro.truncated if with_trunc else None,
+                                       ro.bootstrap if with_init else None, decay=decay)
+    else:
+        rlca.rlca_episodic_prefix_sum(x.view, d.view, trn, init, sums=out.view)
+        ref = oracle.episodic_prefix_sum(ro.value, ro.terminated,
+                                         ro.truncated if with_trunc else None,
+                                         ro.bootstrap if with_init else None)
+    torch.cuda.synchronize()
+    assert out.untouched_outside(SENTINEL), "write outside the output block"
+    return out.view.cpu().numpy().astype(np.float64), ref
+
+
+T_GRID = [1, 2, 3, 7, 8, 9, 16, 31, 32, 33, 100, 255, 256, 257, 511, 512, 1000, 1024,
+          1025, 4096, 5000]
+
+
+@pytest.mark.parametrize("N", [1, 5, 70])
+@pytest.mark.parametrize("T", T_GRID)
+def test_forward_shape_grid(N, T):
+    ro = sr.generic(N, T, seed=N * 7 + T, p_term=0.03, p_trunc=0.02)
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind)
+        assert_parity({"o": g}, {"o": r}, f"{kind} N={N} T={T}")
+
+
+@pytest.mark.parametrize("decay", [0.0, 0.5, 0.99, 1.0])
+def test_forward_decays_and_options(decay):
+    ro = sr.generic(9, 1300, seed=3, p_term=0.01, p_trunc=0.01)
+    for with_trunc in (True, False):
+        for with_init in (True, False):
+            g, r = run_both(ro, "trace", decay=decay, with_trunc=with_trunc,
+                            with_init=with_init)
+            assert_parity({"o": g}, {"o": r}, f"decay={decay} {with_trunc} {with_init}")
+
+
+@pytest.mark.parametrize("pattern", ["all_done", "none", "done_at_0", "done_at_last",
+                                     "every_other"])
+def test_forward_flag_patterns(pattern):
+    ro = sr.generic(6, 777, seed=4)
+    term = np.zeros_like(ro.terminated)
+    if pattern == "all_done":
+        term[:] = 1
+    elif pattern == "done_at_0":
+        term[:, 0] = 1
+    elif pattern == "done_at_last":
+        term[:, -1] = 1
+    elif pattern == "every_other":
+        term[:, ::2] = 1
+    ro.terminated = term
+    ro.truncated = np.zeros_like(term)
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind)
+        assert_parity({"o": g}, {"o": r}, f"{kind} {pattern}")
+
+
+@pytest.mark.parametrize("ld_extra,offset", [(0, 0), (4, 0), (3, 0), (0, 1), (5, 3)])
+@pytest.mark.parametrize("T", [12, 256, 1500])
+def test_forward_layouts(ld_extra, offset, T):
+    ro = sr.generic(3, T, seed=5 + T)
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind, ld=T + ld_extra, offset=offset)
+        assert_parity({"o": g}, {"o": r}, f"{kind} ld=T+{ld_extra} off={offset}")
+
+
+@pytest.mark.parametrize("T", [200, 3000])
+def test_forward_nan_stays_in_its_episode(T):
+    ro = sr.generic(3, T, seed=6, p_term=0.01, p_trunc=0.01)
+    clean, _ = run_both(ro, "trace")
+    n, k = 2, T // 2
+    ro.value[n, k] = np.nan
+    dirty, _ = run_both(ro, "trace")
+    e = k
+    while e + 1 < T and not (ro.terminated[n, e] or ro.truncated[n, e]):
+        e += 1
+    a, b = clean.copy(), dirty.copy()
+    a[n, k:e + 1] = b[n, k:e + 1] = 0.0
+    assert np.array_equal(a, b)
+    assert np.isnan(dirty[n, k:e + 1]).all()
+
+
+def test_forward_workload_sizes():
+    """Full-size rollouts shaped like the bench workload and the long Retrace one."""
+    for N, T in ((4096, 1024), (2048, 4096)):
+        ro = sr.generic(N, T, seed=8, p_term=0.005, p_trunc=0.002)
+        for kind in ("trace", "sum"):
+            g, r = run_both(ro, kind)
+            assert_parity({"o": g}, {"o": r}, f"{kind} {N}x{T}")
