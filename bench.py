@@ -42,6 +42,8 @@ WORKLOADS = {
     "td_lambda": "TD(lambda=0.9), fp32, num_envs=4096, seq_len=1024 (rates of the [4096,128] return/TD workload)",
     "vtrace": "V-trace, fp32, num_envs=4096, seq_len=1024 (rates of the [8192,256] V-trace workload)",
     "retrace": "Retrace, fp32, num_envs=4096, seq_len=1024 (rates of the [2048,4096] Retrace workload)",
+    "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
+    "prefix_sum": "episodic prefix sum (forward scan), fp32, num_envs=4096, seq_len=1024",
 }
 KERNELS = {
     "gae": "credit_warp_stream_kernel<GAE> (warp-owned rows, per-warp TMA ring)",
@@ -49,6 +51,8 @@ KERNELS = {
     "td_lambda": "credit_scan_kernel<TD(lambda), whole-row CTA tiles>",
     "vtrace": "credit_scan_kernel<V-trace, whole-row CTA tiles>",
     "retrace": "credit_scan_kernel<Retrace, whole-row CTA tiles>",
+    "trace": "credit_forward_kernel (warp-owned rows, forward chunks)",
+    "prefix_sum": "credit_forward_kernel (warp-owned rows, forward chunks)",
 }
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
@@ -87,11 +91,15 @@ def algorithmic_bytes(est: str, ro) -> int:
     (truncation values only where a step is truncated and not terminated; per-env
     bootstrap values once) and every output written once."""
     n = ro.N * ro.T
-    f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4}[est]
-    outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1}[est]
+    f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
+              "prefix_sum": 1}[est]
+    outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
+            "prefix_sum": 1}[est]
     b = n * (4 * f32_in + 1 + 4 * outs)
     if ro.truncated is not None:
-        b += n + 4 * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
+        b += n
+        if est not in ("trace", "prefix_sum"):  # forward scans read no truncation values
+            b += 4 * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
     if ro.bootstrap is not None:
         b += 4 * ro.N
     return b
@@ -101,6 +109,8 @@ def workload_inputs(est: str, N: int, T: int, seed: int):
     """The seeded workload each estimator is quoted on, at [N, T]."""
     if est == "gae":
         return sr.gae_trunc(N=N, T=T, seed=seed)
+    if est in ("trace", "prefix_sum"):
+        return sr.traces(N=N, T=T, seed=seed)
     if est in ("return", "td_lambda"):
         return sr.return_td(N=N, T=T, seed=seed)
     if est == "vtrace":
@@ -238,9 +248,15 @@ def launch(rlca, est, s, params):
                          lam=params["lam"], rho_bar=params["rho_bar"],
                          c_bar=params["c_bar"], pg_rho_bar=params["pg_rho_bar"],
                          vs=s.out0, pg_advantages=s.out1)
-    else:
+    elif est == "retrace":
         rlca.rlca_retrace(s.reward, s.q_taken, s.expected_q, s.rho, **fl,
                           bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0)
+    elif est == "trace":
+        rlca.rlca_eligibility_trace(s.value, s.terminated, s.truncated, s.bootstrap,
+                                    decay=params["decay"], traces=s.out0)
+    else:
+        rlca.rlca_episodic_prefix_sum(s.value, s.terminated, s.truncated, s.bootstrap,
+                                      sums=s.out0)
 
 
 def est_params(est, ro):
@@ -280,7 +296,7 @@ def n_sets_for(bytes_per_set):
 def per_estimator_roofline(torch, rlca, device, peak):
     """Each estimator alone at [4096, 1024] on its own workload's distributions."""
     out = {}
-    for est in ("return", "td_lambda", "gae", "vtrace", "retrace"):
+    for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "trace", "prefix_sum"):
         ro = workload_inputs(est, N_ENVS, SEQ_LEN, seed=100)
         params = est_params(est, ro)
         nbytes = algorithmic_bytes(est, ro)

@@ -1,30 +1,41 @@
 // Forward scans (eligibility traces, episodic prefix sums) in a translation unit of
-// their own: warp-owned rows, walked from the first step to the last.
+// their own, walked from the first step to the last.
 #include "forward.cuh"
 #include "launch.cuh"
 
 namespace rlca {
 
+// Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows: CTA tiles of
+// 1024 steps (whole rows, or a row walked tile by tile), which load a whole tile at once.
 template <bool VEC, bool TRUNC>
 cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * kItems;
-    int64_t jobs;
     if (p.T <= CH) {
         const int t_pad = (p.T + kItems - 1) / kItems * kItems;
         p.segs = 1;
         p.chunks_per_row = t_pad / kItems;
         p.rows_per_tile = CH / t_pad;
-        jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
-    } else {
-        p.segs = (p.T + CH - 1) / CH;
-        p.chunks_per_row = CH / kItems;
-        p.rows_per_tile = 1;
-        jobs = p.N;
+        const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
+        const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
+        return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+                          32 * kWarpsPerCta, 0, stream, p);
     }
-    const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
-                      32 * kWarpsPerCta, 0, stream, p);
+    if (p.T <= kTile) {
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.segs = 1;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = kTile / t_pad;
+        const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        return launch_pdl(
+            credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows>, grid,
+            kThreads, 0, stream, p);
+    }
+    p.segs = (p.T + kTile - 1) / kTile;
+    p.chunks_per_row = kTile / kItems;
+    p.rows_per_tile = 1;
+    return launch_pdl(credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>,
+                      (unsigned)p.N, kThreads, 0, stream, p);
 }
 
 cudaError_t launch_forward(const Params &p_in, bool vec, cudaStream_t stream)

@@ -34,8 +34,8 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
 
     float x[ITEMS];
     load_items<ITEMS, VEC>(p.reward + off, t0, Te, x);
-    unsigned ended = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
-    if (TRUNC) ended |= load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te);
+    const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
+                                 : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
     const unsigned valid = valid_items<ITEMS>(t0, Te);
 
     // Item j starts afresh when step t0+j-1 ended an episode; the row's first step resets
@@ -103,6 +103,120 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
         for (int s = 0; s < p.segs; ++s)
             carry = forward_chunk<ITEMS, VEC, TRUNC>(p, job, s * CH + lane * ITEMS, true,
                                                      carry, last_ended, &last_ended);
+    }
+}
+
+// ------------------------------------------------------------------ CTA tiles
+
+// One tile of NT * ITEMS steps scanned forward by a CTA: lane composites, warp prefix
+// scans, the NT/32 warp totals combined through shared memory. `carry_in` is A at the
+// step before the tile and `prev_ended` whether that step ended an episode; returns A at
+// the tile's last step and sets *last_ended.
+//
+// A warp's first step starts afresh when the step before it ended an episode. That flag
+// belongs to the previous warp, so the warp scans as if it did not, and the flag is
+// applied after the exchange instead: the warp's carry-in becomes 0 (its first step then
+// equals x exactly) and its total is marked as a reset for the warps after it.
+template <int NT, int ITEMS, bool VEC, bool TRUNC>
+__device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int t0, bool active,
+                                              float carry_in, bool prev_ended, bool *last_ended,
+                                              ScanSmem<NT> &sm, int buf)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int T = p.T;
+    const int Te = active ? T : 0;
+    const int64_t off = active ? row * p.ld : 0;
+
+    float x[ITEMS];
+    load_items<ITEMS, VEC>(p.reward + off, t0, Te, x);
+    const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
+                                 : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
+    const unsigned valid = valid_items<ITEMS>(t0, Te);
+
+    const unsigned prev_lane = __shfl_up_sync(kFullMask, ended >> (ITEMS - 1), 1) & 1u;
+    unsigned reset = ((ended << 1) | (lane == 0 ? 0u : prev_lane)) | ~valid;
+    if (t0 == 0 && active) {
+        reset |= 1u;
+        if (p.boot) x[0] = fmaf(p.gamma, __ldg(p.boot + row), x[0]);
+    }
+    reset &= all_items<ITEMS>();
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j)
+        if (!((valid >> j) & 1u)) x[j] = 0.f;
+
+    const float decay = p.gamma;
+    float a = x[0];
+#pragma unroll
+    for (int j = 1; j < ITEMS; ++j) a = ((reset >> j) & 1u) ? x[j] : fmaf(decay, a, x[j]);
+    Affine incl{a, reset ? kResetB : p.beta_pow};
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Affine y{__shfl_up_sync(kFullMask, incl.a, d), __shfl_up_sync(kFullMask, incl.b, d)};
+        if (lane >= d) incl = affine_compose(incl, y);
+    }
+    Affine excl{__shfl_up_sync(kFullMask, incl.a, 1), __shfl_up_sync(kFullMask, incl.b, 1)};
+    if (lane == 0) excl = affine_identity();
+    if (lane == 31) {
+        sm.a[buf][warp] = incl.a;
+        sm.b[buf][warp] = incl.b;
+        sm.e[buf][warp] = (ended >> (ITEMS - 1)) & 1u;
+    }
+    __syncthreads();
+
+    // Prefix over the warp totals (lane w ends with total_w o ... o total_0); a warp whose
+    // first step follows an episode end contributes a reset.
+    Affine tw = affine_identity();
+    if (lane < NW) {
+        const bool fresh = lane == 0 ? prev_ended : sm.e[buf][lane - 1] != 0;
+        tw = Affine{sm.a[buf][lane], fresh ? kResetB : sm.b[buf][lane]};
+    }
+#pragma unroll
+    for (int d = 1; d < NW; d <<= 1) {
+        const Affine y{__shfl_up_sync(kFullMask, tw.a, d), __shfl_up_sync(kFullMask, tw.b, d)};
+        if (lane >= d && lane < NW) tw = affine_compose(tw, y);
+    }
+    Affine earlier = shfl_idx(tw, (warp + 31) & 31);
+    if (warp == 0) earlier = affine_identity();
+    const Affine whole = shfl_idx(tw, NW - 1);
+    const bool warp_fresh = warp == 0 ? prev_ended : sm.e[buf][warp - 1] != 0;
+    *last_ended = sm.e[buf][NW - 1] != 0;
+
+    float A[ITEMS];
+    float prev = affine_apply(excl, warp_fresh ? 0.f : affine_apply(earlier, carry_in));
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        prev = ((reset >> j) & 1u) ? x[j] : fmaf(decay, prev, x[j]);
+        A[j] = prev;
+    }
+    if (valid) store_items<ITEMS, VEC>(p.out0 + off, t0, valid, A);
+    return affine_apply(whole, carry_in);
+}
+
+// CTA-tiled forward scan: T <= NT * ITEMS packs whole rows into a tile; longer rows are
+// walked tile by tile from the first, with the carry in registers.
+template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
+__global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
+{
+    __shared__ ScanSmem<NT> sm;
+    grid_dependency_sync();
+    constexpr int TILE = NT * ITEMS;
+    if (TL == Tiling::kRows) {
+        const int local_row = threadIdx.x / p.chunks_per_row;
+        const int chunk = threadIdx.x - local_row * p.chunks_per_row;
+        const int64_t row = (int64_t)blockIdx.x * p.rows_per_tile + local_row;
+        const bool active = local_row < p.rows_per_tile && row < p.N;
+        bool last_ended = false;
+        forward_tile<NT, ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f, false,
+                                            &last_ended, sm, 0);
+    } else {
+        const int64_t row = blockIdx.x;
+        float carry = 0.f;
+        bool ended = false;
+        for (int s = 0; s < p.segs; ++s)
+            carry = forward_tile<NT, ITEMS, VEC, TRUNC>(p, row, s * TILE + threadIdx.x * ITEMS,
+                                                        true, carry, ended, &ended, sm, s & 1);
     }
 }
 

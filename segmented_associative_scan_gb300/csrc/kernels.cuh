@@ -37,6 +37,7 @@ template <int NT>
 struct ScanSmem {
     float a[2][NT / 32];
     float b[2][NT / 32];
+    unsigned e[2][NT / 32];  // forward scans: whether each warp's last step ended an episode
     float carry;
     unsigned tile;
     unsigned epoch;

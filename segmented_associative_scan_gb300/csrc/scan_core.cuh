@@ -137,6 +137,28 @@ __device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ r
     return bits;
 }
 
+// Bit j set when either flag byte (t0 + j) of row_a or row_b is nonzero: the two flag
+// words are OR-ed before a single decode.
+template <int ITEMS, bool VEC>
+__device__ __forceinline__ unsigned load_flag_bits_or(const uint8_t *__restrict__ row_a,
+                                                      const uint8_t *__restrict__ row_b, int t0,
+                                                      int T)
+{
+    unsigned bits = 0;
+    if (VEC && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k)
+            bits |= nonzero_bytes(ld_stream(reinterpret_cast<const uint32_t *>(row_a + t0) + k) |
+                                  ld_stream(reinterpret_cast<const uint32_t *>(row_b + t0) + k))
+                    << (4 * k);
+    } else {
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j)
+            if (t0 + j < T && (row_a[t0 + j] | row_b[t0 + j]) != 0) bits |= 1u << j;
+    }
+    return bits;
+}
+
 // Store the valid items (bit j of `valid`) of ITEMS consecutive floats.
 template <int ITEMS, bool VEC>
 __device__ __forceinline__ void store_items(float *__restrict__ row, int t0, unsigned valid,

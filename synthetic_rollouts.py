@@ -132,6 +132,17 @@ def retrace(N=2048, T=4096, seed=0):
                    rho=rho, params=dict(gamma=0.99, lam=0.95))
 
 
+def traces(N=4096, T=1024, seed=0):
+    """Forward scans (eligibility traces, episodic prefix sums), fp32: per-step inputs
+    x ~ N(0,1) (in `value`), dones ~ B(0.01), truncations ~ B(0.005), carried-in values
+    ~ N(0,1) (in `bootstrap`), decay = gamma * lambda = 0.99 * 0.95."""
+    term, trunc = _flags(seed, N, T, 0.01, 0.005)
+    return Rollout(N, T, reward=normal(seed, "reward", (N, T)), terminated=term,
+                   truncated=trunc, bootstrap=normal(seed, "bootstrap", (N,)),
+                   value=normal(seed, "value", (N, T)),
+                   params=dict(gamma=0.99, lam=0.95, decay=0.99 * 0.95))
+
+
 # The five workloads, by name, with their full sizes.
 WORKLOADS = {
     "gae_16x128": (gae_small, dict(N=16, T=128)),
