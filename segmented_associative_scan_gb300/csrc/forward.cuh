@@ -9,10 +9,11 @@
 // them, applied in the other time order: a warp prefix scan (shfl_up) instead of a
 // suffix scan, chunks walked from the first to the last.
 //
-// Every warp owns whole rows, as in the warp-owned reverse kernel: several short rows
-// per warp (each row's first step resets and folds in init), or one long row walked in
-// chunks of 32 * ITEMS steps with the carry in a register. No CTA barrier, no shared
-// memory. decay >= 0 (checked on the host), so the reset marker of the scan is exact.
+// Two layouts, as for the reverse scans: warp-owned rows for rows of at most one warp
+// chunk (several short rows per warp, each row's first step resetting and folding in
+// init; no CTA barrier, no shared memory), and CTA tiles of 1024 steps for longer rows
+// (whole rows per tile, or a row walked tile by tile with the carry in registers).
+// decay >= 0 (checked on the host), so the reset marker of the scan is exact.
 #pragma once
 
 #include "kernels.cuh"
