@@ -42,6 +42,7 @@ WORKLOADS = {
     "td_lambda": "TD(lambda=0.9), fp32, num_envs=4096, seq_len=1024 (rates of the [4096,128] return/TD workload)",
     "vtrace": "V-trace, fp32, num_envs=4096, seq_len=1024 (rates of the [8192,256] V-trace workload)",
     "retrace": "Retrace, fp32, num_envs=4096, seq_len=1024 (rates of the [2048,4096] Retrace workload)",
+    "td_multi": "TD(lambda) for lambda in {0, 0.9, 1} fused, fp32, num_envs=4096, seq_len=1024",
     "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
     "prefix_sum": "episodic prefix sum (forward scan), fp32, num_envs=4096, seq_len=1024",
 }
@@ -51,8 +52,9 @@ KERNELS = {
     "td_lambda": "credit_scan_kernel<TD(lambda), whole-row CTA tiles>",
     "vtrace": "credit_scan_kernel<V-trace, whole-row CTA tiles>",
     "retrace": "credit_scan_kernel<Retrace, whole-row CTA tiles>",
-    "trace": "credit_forward_kernel (warp-owned rows, forward chunks)",
-    "prefix_sum": "credit_forward_kernel (warp-owned rows, forward chunks)",
+    "td_multi": "credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)",
+    "trace": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
+    "prefix_sum": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
 }
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
@@ -92,9 +94,9 @@ def algorithmic_bytes(est: str, ro) -> int:
     bootstrap values once) and every output written once."""
     n = ro.N * ro.T
     f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
-              "prefix_sum": 1}[est]
+              "prefix_sum": 1, "td_multi": 2}[est]
     outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
-            "prefix_sum": 1}[est]
+            "prefix_sum": 1, "td_multi": 3}[est]
     b = n * (4 * f32_in + 1 + 4 * outs)
     if ro.truncated is not None:
         b += n
@@ -111,7 +113,7 @@ def workload_inputs(est: str, N: int, T: int, seed: int):
         return sr.gae_trunc(N=N, T=T, seed=seed)
     if est in ("trace", "prefix_sum"):
         return sr.traces(N=N, T=T, seed=seed)
-    if est in ("return", "td_lambda"):
+    if est in ("return", "td_lambda", "td_multi"):
         return sr.return_td(N=N, T=T, seed=seed)
     if est == "vtrace":
         return sr.vtrace(N=N, T=T, seed=seed)
@@ -220,7 +222,7 @@ class DeviceSet:
         self.log_rho, self.q_taken, self.expected_q, self.rho = (
             t(ro.log_rho), t(ro.q_taken), t(ro.expected_q), t(ro.rho))
         z = lambda: torch.empty((ro.N, ro.T), dtype=torch.float32, device=device)
-        self.out0, self.out1 = z(), z()
+        self.out0, self.out1, self.out2 = z(), z(), z()
 
     def clone(self):
         import torch
@@ -251,6 +253,9 @@ def launch(rlca, est, s, params):
     elif est == "retrace":
         rlca.rlca_retrace(s.reward, s.q_taken, s.expected_q, s.rho, **fl,
                           bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0)
+    elif est == "td_multi":
+        rlca.rlca_td_lambda_multi(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
+                                  lams=params["lams"], targets=[s.out0, s.out1, s.out2])
     elif est == "trace":
         rlca.rlca_eligibility_trace(s.value, s.terminated, s.truncated, s.bootstrap,
                                     decay=params["decay"], traces=s.out0)
@@ -296,7 +301,8 @@ def n_sets_for(bytes_per_set):
 def per_estimator_roofline(torch, rlca, device, peak):
     """Each estimator alone at [4096, 1024] on its own workload's distributions."""
     out = {}
-    for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "trace", "prefix_sum"):
+    for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi", "trace",
+                "prefix_sum"):
         ro = workload_inputs(est, N_ENVS, SEQ_LEN, seed=100)
         params = est_params(est, ro)
         nbytes = algorithmic_bytes(est, ro)

@@ -143,6 +143,22 @@ int rlca_retrace(const float *reward, const float *q_taken, const float *expecte
                  void *stream);
 
 /*
+ * TD(lambda) for several lambdas in one pass (fused): the inputs are read from HBM once
+ * and every lambda's targets are scanned on chip and written once (Method section 2:
+ * HBM traffic, not arithmetic, bounds these scans, so sharing the load is what pays).
+ * Each targets[k] equals rlca_td_lambda with lambdas[k] (lambda = 1 gives the discounted
+ * return). lambdas: host array of n_lambdas values in [0, 1]; targets: host array of
+ * n_lambdas device pointers [N, ld], none NULL, overlapping no input and no other target.
+ * 1 <= n_lambdas <= RLCA_TD_LAMBDA_MAX, else RLCA_ERR_PARAM.
+ */
+#define RLCA_TD_LAMBDA_MAX 4
+int rlca_td_lambda_multi(const float *reward, const float *value, const uint8_t *terminated,
+                         const uint8_t *truncated, const float *trunc_value,
+                         const float *bootstrap, float gamma, const float *lambdas,
+                         int n_lambdas, int64_t N, int64_t T, int64_t ld,
+                         float *const *targets, void *stream);
+
+/*
  * Forward-time scans (Method section 1: eligibility traces are the forward-time mirror
  * of the recurrence; episodic prefix sums are among the estimators it covers).
  *   A_t = x_t + decay * A_{t-1} inside an episode; A_t = x_t at a step whose previous

@@ -39,6 +39,8 @@ SIGNATURES = {
                      _P, _P], ctypes.c_int),
     "rlca_retrace": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I64, _I64, _I64, _P, _P],
                      ctypes.c_int),
+    "rlca_td_lambda_multi": ([_P, _P, _P, _P, _P, _P, _F, _P, ctypes.c_int, _I64, _I64, _I64,
+                              _P, _P], ctypes.c_int),
     "rlca_eligibility_trace": ([_P, _P, _P, _P, _F, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "rlca_episodic_prefix_sum": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "rlca_workspace_bytes": ([_I64, _I64], ctypes.c_size_t),
@@ -253,6 +255,26 @@ def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
     return q_ret
 
 
+def rlca_td_lambda_multi(reward, value, terminated, truncated=None, trunc_value=None,
+                         bootstrap=None, gamma=0.99, lams=(0.0, 0.9, 1.0), targets=None):
+    """TD(lambda) targets for several lambdas (at most 4) from one read of the inputs.
+    Returns a list of [N, T] tensors, one per lambda."""
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+            g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    lams = [float(x) for x in lams]
+    if targets is None:
+        targets = [None] * len(lams)
+    targets = [g.out(t, f"targets[{k}]") for k, t in enumerate(targets)]
+    lam_arr = (ctypes.c_float * len(lams))(*lams)
+    out_arr = (ctypes.c_void_p * len(lams))(*[t.data_ptr() or None for t in targets])
+    _check("rlca_td_lambda_multi", lib().rlca_td_lambda_multi(
+        *args, gamma, lam_arr, len(lams), g.N, g.T, g.ld, out_arr, _stream(g.device)))
+    return targets
+
+
 def rlca_eligibility_trace(x, terminated, truncated=None, init=None, decay=0.95,
                            traces=None):
     """Forward accumulating trace e_t = x_t + decay e_{t-1}, fresh after an episode ends,
@@ -283,5 +305,6 @@ td_lambda = rlca_td_lambda
 gae = rlca_gae
 vtrace = rlca_vtrace
 retrace = rlca_retrace
+td_lambda_multi = rlca_td_lambda_multi
 eligibility_trace = rlca_eligibility_trace
 episodic_prefix_sum = rlca_episodic_prefix_sum

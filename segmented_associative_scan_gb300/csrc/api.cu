@@ -218,6 +218,40 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
 }
 
+int td_lambda_multi(const float *reward, const float *value, const uint8_t *terminated,
+                    const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
+                    float gamma, const float *lambdas, int n_lambdas, int64_t N, int64_t T,
+                    int64_t ld, float *const *targets, void *stream)
+{
+    if (bad_gamma(gamma)) return RLCA_ERR_PARAM;
+    if (n_lambdas < 1 || n_lambdas > RLCA_TD_LAMBDA_MAX) return RLCA_ERR_PARAM;
+    if (!lambdas || !targets) return RLCA_ERR_NULL;
+    for (int k = 0; k < n_lambdas; ++k)
+        if (bad_lambda(lambdas[k])) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambdas[0], N, T, ld);
+    p.value = value;
+    p.multi.count = n_lambdas;
+    float *outs[RLCA_TD_LAMBDA_MAX] = {};
+    for (int k = 0; k < n_lambdas; ++k) {
+        p.multi.gamma_lambda[k] = gamma * lambdas[k];
+        p.multi.gamma_one_m_lambda[k] = gamma * (1.f - lambdas[k]);
+        p.multi.out[k] = outs[k] = targets[k];
+    }
+    p.out0 = targets[0];
+    // Every target is required (an empty problem needs none).
+    bool empty = false;
+    if (check_shape(N, T, ld, &empty) == RLCA_OK && !empty)
+        for (int k = 0; k < n_lambdas; ++k)
+            if (!outs[k]) return RLCA_ERR_NULL;
+    const float *in[] = {reward, value};
+    auto launch = [](const Params &q, bool vec, bool, cudaStream_t s) {
+        return rlca::launch_td_multi(q, vec, s);
+    };
+    return validate_and_launch(p, in, 2, outs, n_lambdas, Workspace{nullptr, 0}, launch,
+                               stream);
+}
+
 // Forward scans: x and flags as the reverse estimators' reward and flags; `init` is the
 // per-env value carried into the window (nullable); decay >= 0 and finite.
 int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *truncated,
@@ -383,6 +417,16 @@ int rlca_retrace_ex(const float *reward, const float *q_taken, const float *expe
     return retrace(reward, q_taken, expected_q, rho, terminated, truncated, trunc_value,
                    bootstrap_ev, gamma, lambda, N, T, ld, q_ret,
                    Workspace{workspace, workspace_bytes}, stream);
+}
+
+int rlca_td_lambda_multi(const float *reward, const float *value, const uint8_t *terminated,
+                         const uint8_t *truncated, const float *trunc_value,
+                         const float *bootstrap, float gamma, const float *lambdas,
+                         int n_lambdas, int64_t N, int64_t T, int64_t ld,
+                         float *const *targets, void *stream)
+{
+    return td_lambda_multi(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambdas, n_lambdas, N, T, ld, targets, stream);
 }
 
 int rlca_eligibility_trace(const float *x, const uint8_t *terminated,

@@ -7,4 +7,41 @@ cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStr
 {
     return launch_estimator<Est::kTdLambda>(p, vec, streamable, stream);
 }
+// Fused TD(lambda) for several lambdas: whole-row CTA tiles, or the row loop.
+template <bool VEC, bool TRUNC>
+cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
+{
+    if (p.T <= kTile) {
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = kTile / t_pad;
+        p.segs = 1;
+        const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        return launch_pdl(credit_td_multi_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows>,
+                          grid, kThreads, 0, stream, p);
+    }
+    p.chunks_per_row = kTile / kItems;
+    p.rows_per_tile = 1;
+    p.segs = (p.T + kTile - 1) / kTile;
+    return launch_pdl(credit_td_multi_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>,
+                      (unsigned)p.N, kThreads, 0, stream, p);
+}
+
+cudaError_t launch_td_multi(const Params &p_in, bool vec, cudaStream_t stream)
+{
+    Params p = p_in;
+    for (int k = 0; k < p.multi.count; ++k) {
+        const float beta = p.multi.gamma_lambda[k];
+        float pw = beta;
+        for (int i = 1; i < kItems; ++i) pw = beta * pw;
+        p.multi.beta_pow[k] = pw;
+    }
+    const bool trunc = p.trunc != nullptr;
+    if (vec)
+        return trunc ? launch_td_multi_variant<true, true>(p, stream)
+                     : launch_td_multi_variant<true, false>(p, stream);
+    return trunc ? launch_td_multi_variant<false, true>(p, stream)
+                 : launch_td_multi_variant<false, false>(p, stream);
+}
+
 }  // namespace rlca

@@ -28,6 +28,16 @@ namespace rlca {
 
 enum class Est : int { kReturn = 0, kTdLambda = 1, kGae = 2, kVtrace = 3, kRetrace = 4 };
 
+// Fused TD(lambda) for several lambdas from one read of the inputs (at most 4).
+constexpr int kMaxLambdas = 4;
+struct MultiLambda {
+    int count;
+    float gamma_lambda[kMaxLambdas];
+    float gamma_one_m_lambda[kMaxLambdas];
+    float beta_pow[kMaxLambdas];
+    float *out[kMaxLambdas];
+};
+
 // Kernel arguments, passed by value.
 struct Params {
     const float *reward;
@@ -60,6 +70,7 @@ struct Params {
     int spin_limit;   // consecutive empty polls of a later tile before giving up
     int stall;        // testing only: nonzero = tiles never publish their state
     int forward;      // host-side only: a forward scan (truncation needs no values)
+    MultiLambda multi;  // fused TD(lambda) only
 };
 
 template <Est E>

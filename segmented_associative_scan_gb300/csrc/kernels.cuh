@@ -275,6 +275,48 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
     }
 }
 
+// ------------------------------------------------------ fused TD(lambda) (several)
+
+// TD(lambda) for p.multi.count lambdas from one load of a tile: the chunk is read once,
+// then built, scanned and stored once per lambda (each scan alternates the shared
+// buffers, so consecutive scans never race on them).
+template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
+__global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
+{
+    __shared__ ScanSmem<NT> sm;
+    grid_dependency_sync();
+    constexpr int TILE = NT * ITEMS;
+    int call = 0;
+    auto tile = [&](int64_t row, int t0, bool active, float (&carry)[kMaxLambdas]) {
+        Chunk<ITEMS> c;
+        load_chunk<Est::kTdLambda, ITEMS, VEC, TRUNC>(p, row, t0, active, threadIdx.x & 31, c);
+#pragma unroll
+        for (int k = 0; k < kMaxLambdas; ++k) {
+            if (k < p.multi.count) {
+                Params q = p;
+                q.gamma_lambda = p.multi.gamma_lambda[k];
+                q.gamma_one_m_lambda = p.multi.gamma_one_m_lambda[k];
+                q.beta_pow = p.multi.beta_pow[k];
+                q.out0 = p.multi.out[k];
+                carry[k] = scan_chunk<Est::kTdLambda, NT, ITEMS, VEC, false>(q, c, row, t0,
+                                                                          carry[k], sm,
+                                                                          call & 1);
+                ++call;
+            }
+        }
+    };
+    float carry[kMaxLambdas] = {0.f, 0.f, 0.f, 0.f};
+    if (TL == Tiling::kRows) {
+        const int local_row = threadIdx.x / p.chunks_per_row;
+        const int chunk = threadIdx.x - local_row * p.chunks_per_row;
+        const int64_t row = (int64_t)blockIdx.x * p.rows_per_tile + local_row;
+        tile(row, chunk * ITEMS, local_row < p.rows_per_tile && row < p.N, carry);
+    } else {
+        const int64_t row = blockIdx.x;
+        for (int s = p.segs - 1; s >= 0; --s) tile(row, s * TILE + threadIdx.x * ITEMS, true, carry);
+    }
+}
+
 // ----------------------------------------------------------- warp-owned rows (kWarp)
 
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane

@@ -208,6 +208,8 @@ cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStr
 cudaError_t launch_gae(const Params &p, bool vec, bool streamable, cudaStream_t stream);
 cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
 cudaError_t launch_retrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+// Fused TD(lambda) for p.multi.count lambdas (outputs in p.multi.out).
+cudaError_t launch_td_multi(const Params &p, bool vec, cudaStream_t stream);
 // Forward scans: p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
 cudaError_t launch_forward(const Params &p, bool vec, cudaStream_t stream);
 

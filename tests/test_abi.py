@@ -126,3 +126,21 @@ def test_workspace_size_and_validation(lib):
     assert lib.rlca_testing_lookback_stall(fake(1), fake(2), 4, 1000, fake(3), ws, 10**6, 8,
                                            None) == WORKSPACE  # one tile per row
     assert lib.rlca_workspace_check(None, None) == NULL
+
+
+def test_td_lambda_multi_validation(lib):
+    lam = (ctypes.c_float * 5)(0.0, 0.5, 0.9, 1.0, 0.3)
+    outs = (ctypes.c_void_p * 5)(fake(4), fake(5), fake(6), fake(7), fake(8))
+    call = lambda n, lams=lam, tg=outs, g=0.99: lib.rlca_td_lambda_multi(
+        fake(1), fake(2), fake(3), None, None, None, g, lams, n, 4, 64, 64, tg, None)
+    assert call(0) == PARAM and call(5) == PARAM
+    assert call(2, lams=None) == NULL and call(2, tg=None) == NULL
+    bad = (ctypes.c_float * 2)(0.5, 1.5)
+    assert call(2, lams=bad) == PARAM
+    assert call(2, g=-1.0) == PARAM
+    holes = (ctypes.c_void_p * 3)(fake(4), None, fake(6))
+    assert call(3, tg=holes) == NULL
+    same = (ctypes.c_void_p * 2)(fake(4), fake(4))
+    assert call(2, tg=same) == ALIAS
+    into_input = (ctypes.c_void_p * 2)(fake(4), fake(2))
+    assert call(2, tg=into_input) == ALIAS
