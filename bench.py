@@ -43,6 +43,8 @@ WORKLOADS = {
     "vtrace": "V-trace, fp32, num_envs=4096, seq_len=1024 (rates of the [8192,256] V-trace workload)",
     "retrace": "Retrace, fp32, num_envs=4096, seq_len=1024 (rates of the [2048,4096] Retrace workload)",
     "td_multi": "TD(lambda) for lambda in {0, 0.9, 1} fused, fp32, num_envs=4096, seq_len=1024",
+    "gae_bf16": "GAE with truncation bootstrapping, bf16 inputs / fp32 math and outputs, "
+                "num_envs=4096, seq_len=1024",
     "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
     "prefix_sum": "episodic prefix sum (forward scan), fp32, num_envs=4096, seq_len=1024",
 }
@@ -53,6 +55,7 @@ KERNELS = {
     "vtrace": "credit_scan_kernel<V-trace, whole-row CTA tiles>",
     "retrace": "credit_scan_kernel<Retrace, whole-row CTA tiles>",
     "td_multi": "credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)",
+    "gae_bf16": "credit_scan_kernel<GAE, bf16 inputs, whole-row CTA tiles>",
     "trace": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
     "prefix_sum": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
 }
@@ -94,14 +97,15 @@ def algorithmic_bytes(est: str, ro) -> int:
     bootstrap values once) and every output written once."""
     n = ro.N * ro.T
     f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
-              "prefix_sum": 1, "td_multi": 2}[est]
+              "prefix_sum": 1, "td_multi": 2, "gae_bf16": 2}[est]
     outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
-            "prefix_sum": 1, "td_multi": 3}[est]
-    b = n * (4 * f32_in + 1 + 4 * outs)
+            "prefix_sum": 1, "td_multi": 3, "gae_bf16": 2}[est]
+    in_bytes = 2 if est.endswith("_bf16") else 4
+    b = n * (in_bytes * f32_in + 1 + 4 * outs)
     if ro.truncated is not None:
         b += n
         if est not in ("trace", "prefix_sum"):  # forward scans read no truncation values
-            b += 4 * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
+            b += in_bytes * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
     if ro.bootstrap is not None:
         b += 4 * ro.N
     return b
@@ -109,7 +113,7 @@ def algorithmic_bytes(est: str, ro) -> int:
 
 def workload_inputs(est: str, N: int, T: int, seed: int):
     """The seeded workload each estimator is quoted on, at [N, T]."""
-    if est == "gae":
+    if est in ("gae", "gae_bf16"):
         return sr.gae_trunc(N=N, T=T, seed=seed)
     if est in ("trace", "prefix_sum"):
         return sr.traces(N=N, T=T, seed=seed)
@@ -210,12 +214,18 @@ def job_throughput(world: int, N: int, T: int, steps: int, ms_max: float) -> flo
 # --------------------------------------------------------------------------- GPU arm
 
 class DeviceSet:
-    """One batch resident in HBM plus its output buffers."""
+    """One batch resident in HBM plus its output buffers (data inputs in `data_dtype`)."""
 
-    def __init__(self, ro, device):
+    def __init__(self, ro, device, data_dtype=None):
         import torch
         self.ro = ro
-        t = lambda a: None if a is None else torch.from_numpy(a).to(device)
+
+        def t(a):
+            if a is None:
+                return None
+            x = torch.from_numpy(a).to(device)
+            return x.to(data_dtype) if data_dtype is not None and x.is_floating_point() \
+                and x.dim() == 2 else x
         self.reward, self.value = t(ro.reward), t(ro.value)
         self.terminated, self.truncated = t(ro.terminated), t(ro.truncated)
         self.trunc_value, self.bootstrap = t(ro.trunc_value), t(ro.bootstrap)
@@ -236,7 +246,7 @@ def launch(rlca, est, s, params):
     fl = dict(terminated=s.terminated, truncated=s.truncated,
               trunc_value=s.trunc_value if s.truncated is not None else None)
     g = params["gamma"]
-    if est == "gae":
+    if est in ("gae", "gae_bf16"):
         rlca.rlca_gae(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
                       lam=params["lam"], advantages=s.out0, returns=s.out1)
     elif est == "return":
@@ -302,11 +312,11 @@ def per_estimator_roofline(torch, rlca, device, peak):
     """Each estimator alone at [4096, 1024] on its own workload's distributions."""
     out = {}
     for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi", "trace",
-                "prefix_sum"):
+                "prefix_sum", "gae_bf16"):
         ro = workload_inputs(est, N_ENVS, SEQ_LEN, seed=100)
         params = est_params(est, ro)
         nbytes = algorithmic_bytes(est, ro)
-        base = DeviceSet(ro, device)
+        base = DeviceSet(ro, device, torch.bfloat16 if est.endswith("_bf16") else None)
         sets = [base] + [base.clone() for _ in range(n_sets_for(nbytes) - 1)]
         for i in range(3):
             launch(rlca, est, sets[i % len(sets)], params)

@@ -180,6 +180,48 @@ int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
                              int64_t ld, float *sums, void *stream);
 
 /*
+ * bf16 inputs. The same estimators with every per-step data input (rewards, values,
+ * log-ratios, ratios, Q-values, truncation values, x) given as bf16: uint16_t holding the
+ * bf16 bit pattern (a torch.bfloat16 tensor qualifies). Each value widens to fp32
+ * exactly and all arithmetic is fp32, so the results equal the fp32 entry points' on
+ * the widened inputs up to rounding order. Per-env bootstrap / init values and all
+ * outputs stay fp32. Rows take 128-bit loads when ld % 8 == 0 and every input base is
+ * 16-byte aligned. Arguments, layouts and errors otherwise as the fp32 entry points.
+ * This halves the bytes of each data input; the pages note that data formats other
+ * than the standard one need more work (technical summary, lay text on limitations).
+ */
+int rlca_discounted_return_bf16(const uint16_t *reward, const uint8_t *terminated,
+                                const uint8_t *truncated, const uint16_t *trunc_value,
+                                const float *bootstrap, float gamma, int64_t N, int64_t T,
+                                int64_t ld, float *returns, void *stream);
+int rlca_td_lambda_bf16(const uint16_t *reward, const uint16_t *value,
+                        const uint8_t *terminated, const uint8_t *truncated,
+                        const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                        float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
+                        void *stream);
+int rlca_gae_bf16(const uint16_t *reward, const uint16_t *value, const uint8_t *terminated,
+                  const uint8_t *truncated, const uint16_t *trunc_value, const float *bootstrap,
+                  float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+                  float *advantages, float *returns, void *stream);
+int rlca_vtrace_bf16(const uint16_t *reward, const uint16_t *value, const uint16_t *log_rho,
+                     const uint8_t *terminated, const uint8_t *truncated,
+                     const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                     float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                     int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream);
+int rlca_retrace_bf16(const uint16_t *reward, const uint16_t *q_taken,
+                      const uint16_t *expected_q, const uint16_t *rho,
+                      const uint8_t *terminated, const uint8_t *truncated,
+                      const uint16_t *trunc_value, const float *bootstrap_ev, float gamma,
+                      float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                      void *stream);
+int rlca_eligibility_trace_bf16(const uint16_t *x, const uint8_t *terminated,
+                                const uint8_t *truncated, const float *init, float decay,
+                                int64_t N, int64_t T, int64_t ld, float *traces, void *stream);
+int rlca_episodic_prefix_sum_bf16(const uint16_t *x, const uint8_t *terminated,
+                                  const uint8_t *truncated, const float *init, int64_t N,
+                                  int64_t T, int64_t ld, float *sums, void *stream);
+
+/*
  * Long sequences: tiles scanned in parallel with decoupled look-back.
  *
  * The kernels scan tiles of 1024 steps. When T > 1024 a row spans several tiles. The

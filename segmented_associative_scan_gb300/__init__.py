@@ -8,7 +8,8 @@ fallback: if the library is not built, every call raises.
 The functions carry the names of the C entry points (``include/rlca.h``) and take
 torch tensors:
   - per-step tensors: CUDA, 2-D [N, T], unit stride along T, all with the same row
-    stride; float32 data, uint8 or bool flags;
+    stride; float32 data (or all bfloat16, which selects the _bf16 entry points), uint8
+    or bool flags;
   - per-env bootstrap values: CUDA float32 [N] (optional);
   - outputs are allocated (same row stride as the inputs) unless passed in.
 Work is enqueued on ``torch.cuda.current_stream()``; nothing synchronises.
@@ -49,6 +50,10 @@ SIGNATURES = {
                                      _P], ctypes.c_int),
 }
 SIGNATURES["rlca_gae_noalloc"] = SIGNATURES["rlca_gae"]
+# bf16-input variants: the same argument list (the data pointers hold bf16).
+for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
+              "rlca_retrace", "rlca_eligibility_trace", "rlca_episodic_prefix_sum"):
+    SIGNATURES[_name + "_bf16"] = SIGNATURES[_name]
 # The _ex variants take (workspace, workspace_bytes) before the stream.
 for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
               "rlca_retrace"):
@@ -162,8 +167,20 @@ def workspace_check(workspace: torch.Tensor) -> int:
     return int(lib().rlca_workspace_check(workspace.data_ptr(), _stream(workspace.device)))
 
 
-def _call(name, args, workspace, stream):
-    """Call the plain entry point, or its _ex variant when a workspace is given."""
+def _data_dtype(t):
+    """Per-step data inputs are all fp32 or all bf16; returns the allowed dtype tuple."""
+    if t.dtype == torch.bfloat16:
+        return (torch.bfloat16,)
+    return _F32
+
+
+def _call(name, args, workspace, stream, bf16=False):
+    """Call the plain entry point, its _bf16 variant for bf16 inputs, or its _ex variant
+    when a workspace is given."""
+    if bf16:
+        if workspace is not None:
+            raise ValueError("the bf16 entry points take no workspace")
+        return getattr(lib(), name + "_bf16")(*args, stream)
     if workspace is None:
         return getattr(lib(), name)(*args, stream)
     if not workspace.is_cuda or workspace.dtype != torch.uint8:
@@ -175,28 +192,30 @@ def _call(name, args, workspace, stream):
 def rlca_discounted_return(reward, terminated, truncated=None, trunc_value=None,
                            bootstrap=None, gamma=0.99, returns=None, workspace=None):
     g = _Rows(reward)
-    args = (g.ptr(reward, "reward", _F32), g.ptr(terminated, "terminated", _FLAG),
+    dd = _data_dtype(reward)
+    args = (g.ptr(reward, "reward", dd), g.ptr(terminated, "terminated", _FLAG),
             g.ptr(truncated, "truncated", _FLAG, True),
-            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.ptr(trunc_value, "trunc_value", dd, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     returns = g.out(returns, "returns")
     _check("rlca_discounted_return", _call(
         "rlca_discounted_return", (*args, gamma, g.N, g.T, g.ld, returns.data_ptr() or None),
-        workspace, _stream(g.device)))
+        workspace, _stream(g.device), dd != _F32))
     return returns
 
 
 def rlca_td_lambda(reward, value, terminated, truncated=None, trunc_value=None,
                    bootstrap=None, gamma=0.99, lam=0.95, targets=None, workspace=None):
     g = _Rows(reward)
-    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+    dd = _data_dtype(reward)
+    args = (g.ptr(reward, "reward", dd), g.ptr(value, "value", dd),
             g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
-            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.ptr(trunc_value, "trunc_value", dd, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     targets = g.out(targets, "targets")
     _check("rlca_td_lambda", _call(
         "rlca_td_lambda", (*args, gamma, lam, g.N, g.T, g.ld, targets.data_ptr() or None),
-        workspace, _stream(g.device)))
+        workspace, _stream(g.device), dd != _F32))
     return targets
 
 
@@ -204,16 +223,17 @@ def rlca_gae(reward, value, terminated, truncated=None, trunc_value=None, bootst
              gamma=0.99, lam=0.95, advantages=None, returns=None, want_returns=True,
              workspace=None):
     g = _Rows(reward)
-    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+    dd = _data_dtype(reward)
+    args = (g.ptr(reward, "reward", dd), g.ptr(value, "value", dd),
             g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
-            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.ptr(trunc_value, "trunc_value", dd, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     advantages = g.out(advantages, "advantages")
     returns = g.out(returns, "returns") if (want_returns or returns is not None) else None
     _check("rlca_gae", _call(
         "rlca_gae", (*args, gamma, lam, g.N, g.T, g.ld, advantages.data_ptr() or None,
                      returns.data_ptr() or None if returns is not None else None),
-        workspace, _stream(g.device)))
+        workspace, _stream(g.device), dd != _F32))
     return advantages, returns
 
 
@@ -221,10 +241,11 @@ def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=
                 bootstrap=None, gamma=0.99, lam=1.0, rho_bar=1.0, c_bar=1.0,
                 pg_rho_bar=None, vs=None, pg_advantages=None, want_pg=True, workspace=None):
     g = _Rows(reward)
-    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
-            g.ptr(log_rho, "log_rho", _F32), g.ptr(terminated, "terminated", _FLAG),
+    dd = _data_dtype(reward)
+    args = (g.ptr(reward, "reward", dd), g.ptr(value, "value", dd),
+            g.ptr(log_rho, "log_rho", dd), g.ptr(terminated, "terminated", _FLAG),
             g.ptr(truncated, "truncated", _FLAG, True),
-            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.ptr(trunc_value, "trunc_value", dd, truncated is None),
             g.vec_ptr(bootstrap, "bootstrap"))
     vs = g.out(vs, "vs")
     pg = g.out(pg_advantages, "pg_advantages") if (want_pg or pg_advantages is not None) \
@@ -235,7 +256,7 @@ def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=
         "rlca_vtrace", (*args, gamma, lam, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld,
                         vs.data_ptr() or None,
                         pg.data_ptr() or None if pg is not None else None),
-        workspace, _stream(g.device)))
+        workspace, _stream(g.device), dd != _F32))
     return vs, pg
 
 
@@ -243,15 +264,16 @@ def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
                  trunc_value=None, bootstrap_ev=None, gamma=0.99, lam=0.95, q_ret=None,
                  workspace=None):
     g = _Rows(reward)
-    args = (g.ptr(reward, "reward", _F32), g.ptr(q_taken, "q_taken", _F32),
-            g.ptr(expected_q, "expected_q", _F32), g.ptr(rho, "rho", _F32),
+    dd = _data_dtype(reward)
+    args = (g.ptr(reward, "reward", dd), g.ptr(q_taken, "q_taken", dd),
+            g.ptr(expected_q, "expected_q", dd), g.ptr(rho, "rho", dd),
             g.ptr(terminated, "terminated", _FLAG), g.ptr(truncated, "truncated", _FLAG, True),
-            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.ptr(trunc_value, "trunc_value", dd, truncated is None),
             g.vec_ptr(bootstrap_ev, "bootstrap_ev"))
     q_ret = g.out(q_ret, "q_ret")
     _check("rlca_retrace", _call(
         "rlca_retrace", (*args, gamma, lam, g.N, g.T, g.ld, q_ret.data_ptr() or None),
-        workspace, _stream(g.device)))
+        workspace, _stream(g.device), dd != _F32))
     return q_ret
 
 
@@ -280,22 +302,26 @@ def rlca_eligibility_trace(x, terminated, truncated=None, init=None, decay=0.95,
     """Forward accumulating trace e_t = x_t + decay e_{t-1}, fresh after an episode ends,
     e_{-1} = init."""
     g = _Rows(x)
-    args = (g.ptr(x, "x", _F32), g.ptr(terminated, "terminated", _FLAG),
+    dd = _data_dtype(x)
+    args = (g.ptr(x, "x", dd), g.ptr(terminated, "terminated", _FLAG),
             g.ptr(truncated, "truncated", _FLAG, True), g.vec_ptr(init, "init"))
     traces = g.out(traces, "traces")
-    _check("rlca_eligibility_trace", lib().rlca_eligibility_trace(
-        *args, decay, g.N, g.T, g.ld, traces.data_ptr() or None, _stream(g.device)))
+    _check("rlca_eligibility_trace", _call(
+        "rlca_eligibility_trace", (*args, decay, g.N, g.T, g.ld, traces.data_ptr() or None),
+        None, _stream(g.device), dd != _F32))
     return traces
 
 
 def rlca_episodic_prefix_sum(x, terminated, truncated=None, init=None, sums=None):
     """Forward sum of x within each episode, S_{-1} = init."""
     g = _Rows(x)
-    args = (g.ptr(x, "x", _F32), g.ptr(terminated, "terminated", _FLAG),
+    dd = _data_dtype(x)
+    args = (g.ptr(x, "x", dd), g.ptr(terminated, "terminated", _FLAG),
             g.ptr(truncated, "truncated", _FLAG, True), g.vec_ptr(init, "init"))
     sums = g.out(sums, "sums")
-    _check("rlca_episodic_prefix_sum", lib().rlca_episodic_prefix_sum(
-        *args, g.N, g.T, g.ld, sums.data_ptr() or None, _stream(g.device)))
+    _check("rlca_episodic_prefix_sum", _call(
+        "rlca_episodic_prefix_sum", (*args, g.N, g.T, g.ld, sums.data_ptr() or None),
+        None, _stream(g.device), dd != _F32))
     return sums
 
 

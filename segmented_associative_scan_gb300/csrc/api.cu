@@ -48,9 +48,11 @@ struct Workspace {
 
 // Common validation of inputs, outputs and workspace, then launch.
 // `f32_in` are the required float inputs, `outs` the outputs (outs[0] required).
+// `in_elem`: bytes per element of the per-step data inputs (4 = fp32, 2 = bf16).
 template <typename LaunchFn>
 int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *const *outs,
-                        int n_out, Workspace ws, LaunchFn launch, void *stream)
+                        int n_out, Workspace ws, LaunchFn launch, void *stream,
+                        size_t in_elem = 4)
 {
     // An empty problem is valid whatever the pointers (an empty tensor may have none).
     bool empty = false;
@@ -65,10 +67,10 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
     // Outputs may overlap neither an input nor each other.
     Range in_ranges[8];
     int k = 0;
-    for (int i = 0; i < n_in; ++i) in_ranges[k++] = span(f32_in[i], p.N, p.T, p.ld, 4);
+    for (int i = 0; i < n_in; ++i) in_ranges[k++] = span(f32_in[i], p.N, p.T, p.ld, in_elem);
     in_ranges[k++] = span(p.term, p.N, p.T, p.ld, 1);
     if (p.trunc) in_ranges[k++] = span(p.trunc, p.N, p.T, p.ld, 1);
-    if (p.trunc_value) in_ranges[k++] = span(p.trunc_value, p.N, p.T, p.ld, 4);
+    if (p.trunc_value) in_ranges[k++] = span(p.trunc_value, p.N, p.T, p.ld, in_elem);
     if (p.boot) in_ranges[k++] = span(p.boot, 1, p.N, p.N, 4);
     for (int o = 0; o < n_out; ++o) {
         if (!outs[o]) continue;
@@ -94,14 +96,16 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
         if (p.spin_limit <= 0) p.spin_limit = rlca::kDefaultSpinLimit;
     }
 
-    // 128-bit loads/stores need 16-byte aligned rows: ld % 4 == 0 and aligned bases.
-    bool vec = (p.ld % 4) == 0 && aligned(p.term, 4) && (!p.trunc || aligned(p.trunc, 4));
+    // 128-bit loads/stores need 16-byte aligned rows: ld a multiple of 16 bytes of every
+    // array (ld % 4 == 0 for fp32, ld % 8 == 0 for bf16 inputs) and aligned bases.
+    bool vec = (p.ld % (int64_t)(16 / in_elem)) == 0 && aligned(p.term, 4) &&
+               (!p.trunc || aligned(p.trunc, 4));
     for (int i = 0; i < n_in; ++i) vec = vec && aligned(f32_in[i], 16);
     for (int o = 0; o < n_out; ++o) vec = vec && (!outs[o] || aligned(outs[o], 16));
 
     // The warp-streaming kernel moves chunks with 16-byte bulk copies: every base
     // 16-byte aligned, ld and T multiples of 16, and packed rows contiguous (ld == T).
-    bool streamable = vec && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
+    bool streamable = in_elem == 4 && vec && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
                       (p.T > rlca::kWarpChunk || p.ld == p.T) && aligned(p.term, 16) &&
                       (!p.trunc || aligned(p.trunc, 16));
 
@@ -131,10 +135,18 @@ Params base_params(const float *reward, const uint8_t *term, const uint8_t *trun
     return p;
 }
 
+// bf16 = the per-step data inputs hold bf16 bit patterns (no workspace then).
+// Adapts a bf16 launcher (no streaming kernel) to the launch signature.
+template <typename F>
+auto bf16_launch(F fn)
+{
+    return [fn](const Params &q, bool vec, bool, cudaStream_t s) { return fn(q, vec, s); };
+}
+
 int discounted_return(const float *reward, const uint8_t *terminated, const uint8_t *truncated,
                       const float *trunc_value, const float *bootstrap, float gamma, int64_t N,
                       int64_t T, int64_t ld, float *returns, Workspace ws, void *stream,
-                      int spin_limit = 0, int stall = 0)
+                      int spin_limit = 0, int stall = 0, bool bf16 = false)
 {
     if (bad_gamma(gamma)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma, 1.f,
@@ -144,13 +156,16 @@ int discounted_return(const float *reward, const uint8_t *terminated, const uint
     p.stall = stall;
     const float *in[] = {reward};
     float *out[] = {returns};
+    if (bf16)
+        return validate_and_launch(p, in, 1, out, 1, ws, bf16_launch(rlca::launch_return_bf16),
+                                   stream, 2);
     return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return, stream);
 }
 
 int td_lambda(const float *reward, const float *value, const uint8_t *terminated,
               const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
               float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
-              Workspace ws, void *stream)
+              Workspace ws, void *stream, bool bf16 = false)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -159,13 +174,16 @@ int td_lambda(const float *reward, const float *value, const uint8_t *terminated
     p.out0 = targets;
     const float *in[] = {reward, value};
     float *out[] = {targets};
+    if (bf16)
+        return validate_and_launch(p, in, 2, out, 1, ws,
+                                   bf16_launch(rlca::launch_td_lambda_bf16), stream, 2);
     return validate_and_launch(p, in, 2, out, 1, ws, rlca::launch_td_lambda, stream);
 }
 
 int gae(const float *reward, const float *value, const uint8_t *terminated,
         const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
         float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *advantages,
-        float *returns, Workspace ws, void *stream)
+        float *returns, Workspace ws, void *stream, bool bf16 = false)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -175,6 +193,9 @@ int gae(const float *reward, const float *value, const uint8_t *terminated,
     p.out1 = returns;
     const float *in[] = {reward, value};
     float *out[] = {advantages, returns};
+    if (bf16)
+        return validate_and_launch(p, in, 2, out, 2, ws, bf16_launch(rlca::launch_gae_bf16),
+                                   stream, 2);
     return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae, stream);
 }
 
@@ -182,7 +203,7 @@ int vtrace(const float *reward, const float *value, const float *log_rho,
            const uint8_t *terminated, const uint8_t *truncated, const float *trunc_value,
            const float *bootstrap, float gamma, float lambda, float rho_bar, float c_bar,
            float pg_rho_bar, int64_t N, int64_t T, int64_t ld, float *vs,
-           float *pg_advantages, Workspace ws, void *stream)
+           float *pg_advantages, Workspace ws, void *stream, bool bf16 = false)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda) || bad_clip(rho_bar) || bad_clip(c_bar) ||
         bad_clip(pg_rho_bar))
@@ -198,13 +219,17 @@ int vtrace(const float *reward, const float *value, const float *log_rho,
     p.out1 = pg_advantages;
     const float *in[] = {reward, value, log_rho};
     float *out[] = {vs, pg_advantages};
+    if (bf16)
+        return validate_and_launch(p, in, 3, out, 2, ws, bf16_launch(rlca::launch_vtrace_bf16),
+                                   stream, 2);
     return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace, stream);
 }
 
 int retrace(const float *reward, const float *q_taken, const float *expected_q,
             const float *rho, const uint8_t *terminated, const uint8_t *truncated,
             const float *trunc_value, const float *bootstrap_ev, float gamma, float lambda,
-            int64_t N, int64_t T, int64_t ld, float *q_ret, Workspace ws, void *stream)
+            int64_t N, int64_t T, int64_t ld, float *q_ret, Workspace ws, void *stream,
+            bool bf16 = false)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap_ev, gamma,
@@ -215,6 +240,9 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     p.out0 = q_ret;
     const float *in[] = {reward, q_taken, expected_q, rho};
     float *out[] = {q_ret};
+    if (bf16)
+        return validate_and_launch(p, in, 4, out, 1, ws, bf16_launch(rlca::launch_retrace_bf16),
+                                   stream, 2);
     return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
 }
 
@@ -256,7 +284,7 @@ int td_lambda_multi(const float *reward, const float *value, const uint8_t *term
 // per-env value carried into the window (nullable); decay >= 0 and finite.
 int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *truncated,
                  const float *init, float decay, int64_t N, int64_t T, int64_t ld, float *out,
-                 void *stream)
+                 void *stream, bool bf16 = false)
 {
     if (!std::isfinite(decay) || decay < 0.f) return RLCA_ERR_PARAM;
     Params p = base_params(x, terminated, truncated, nullptr, init, decay, 1.f, N, T, ld);
@@ -265,10 +293,11 @@ int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *trunc
     p.out0 = out;
     const float *in[] = {x};
     float *outs[] = {out};
-    auto launch = [](const Params &q, bool vec, bool, cudaStream_t s) {
-        return rlca::launch_forward(q, vec, s);
+    auto launch = [bf16](const Params &q, bool vec, bool, cudaStream_t s) {
+        return bf16 ? rlca::launch_forward_bf16(q, vec, s) : rlca::launch_forward(q, vec, s);
     };
-    return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream);
+    return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream,
+                               bf16 ? 2 : 4);
 }
 
 constexpr Workspace kNoWorkspace{nullptr, 0};
@@ -442,6 +471,82 @@ int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
 {
     return forward_scan(x, terminated, truncated, init, 1.f, N, T, ld, sums, stream);
 }
+
+// ---- bf16 per-step inputs (bit patterns), fp32 bootstrap values and outputs.
+
+#define RLCA_BF(p) reinterpret_cast<const float *>(p)
+
+int rlca_discounted_return_bf16(const uint16_t *reward, const uint8_t *terminated,
+                                const uint8_t *truncated, const uint16_t *trunc_value,
+                                const float *bootstrap, float gamma, int64_t N, int64_t T,
+                                int64_t ld, float *returns, void *stream)
+{
+    return discounted_return(RLCA_BF(reward), terminated, truncated, RLCA_BF(trunc_value),
+                             bootstrap, gamma, N, T, ld, returns, kNoWorkspace, stream, 0, 0,
+                             true);
+}
+
+int rlca_td_lambda_bf16(const uint16_t *reward, const uint16_t *value,
+                        const uint8_t *terminated, const uint8_t *truncated,
+                        const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                        float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
+                        void *stream)
+{
+    return td_lambda(RLCA_BF(reward), RLCA_BF(value), terminated, truncated,
+                     RLCA_BF(trunc_value), bootstrap, gamma, lambda, N, T, ld, targets,
+                     kNoWorkspace, stream, true);
+}
+
+int rlca_gae_bf16(const uint16_t *reward, const uint16_t *value, const uint8_t *terminated,
+                  const uint8_t *truncated, const uint16_t *trunc_value, const float *bootstrap,
+                  float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+                  float *advantages, float *returns, void *stream)
+{
+    return gae(RLCA_BF(reward), RLCA_BF(value), terminated, truncated, RLCA_BF(trunc_value),
+               bootstrap, gamma, lambda, N, T, ld, advantages, returns, kNoWorkspace, stream,
+               true);
+}
+
+int rlca_vtrace_bf16(const uint16_t *reward, const uint16_t *value, const uint16_t *log_rho,
+                     const uint8_t *terminated, const uint8_t *truncated,
+                     const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                     float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                     int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream)
+{
+    return vtrace(RLCA_BF(reward), RLCA_BF(value), RLCA_BF(log_rho), terminated, truncated,
+                  RLCA_BF(trunc_value), bootstrap, gamma, lambda, rho_bar, c_bar, pg_rho_bar, N,
+                  T, ld, vs, pg_advantages, kNoWorkspace, stream, true);
+}
+
+int rlca_retrace_bf16(const uint16_t *reward, const uint16_t *q_taken,
+                      const uint16_t *expected_q, const uint16_t *rho,
+                      const uint8_t *terminated, const uint8_t *truncated,
+                      const uint16_t *trunc_value, const float *bootstrap_ev, float gamma,
+                      float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                      void *stream)
+{
+    return retrace(RLCA_BF(reward), RLCA_BF(q_taken), RLCA_BF(expected_q), RLCA_BF(rho),
+                   terminated, truncated, RLCA_BF(trunc_value), bootstrap_ev, gamma, lambda, N,
+                   T, ld, q_ret, kNoWorkspace, stream, true);
+}
+
+int rlca_eligibility_trace_bf16(const uint16_t *x, const uint8_t *terminated,
+                                const uint8_t *truncated, const float *init, float decay,
+                                int64_t N, int64_t T, int64_t ld, float *traces, void *stream)
+{
+    return forward_scan(RLCA_BF(x), terminated, truncated, init, decay, N, T, ld, traces, stream,
+                        true);
+}
+
+int rlca_episodic_prefix_sum_bf16(const uint16_t *x, const uint8_t *terminated,
+                                  const uint8_t *truncated, const float *init, int64_t N,
+                                  int64_t T, int64_t ld, float *sums, void *stream)
+{
+    return forward_scan(RLCA_BF(x), terminated, truncated, init, 1.f, N, T, ld, sums, stream,
+                        true);
+}
+
+#undef RLCA_BF
 
 int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, int64_t N,
                                 int64_t T, float *returns, void *workspace,

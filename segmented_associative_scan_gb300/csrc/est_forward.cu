@@ -7,7 +7,7 @@ namespace rlca {
 
 // Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows: CTA tiles of
 // 1024 steps (whole rows, or a row walked tile by tile), which load a whole tile at once.
-template <bool VEC, bool TRUNC>
+template <bool VEC, bool TRUNC, typename TIn = float>
 cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * kItems;
@@ -18,7 +18,7 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         p.rows_per_tile = CH / t_pad;
         const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
         const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-        return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+        return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta, TIn>, grid,
                           32 * kWarpsPerCta, 0, stream, p);
     }
     if (p.T <= kTile) {
@@ -28,17 +28,19 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         p.rows_per_tile = kTile / t_pad;
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
         return launch_pdl(
-            credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows>, grid,
+            credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows, TIn>, grid,
             kThreads, 0, stream, p);
     }
     p.segs = (p.T + kTile - 1) / kTile;
     p.chunks_per_row = kTile / kItems;
     p.rows_per_tile = 1;
-    return launch_pdl(credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>,
-                      (unsigned)p.N, kThreads, 0, stream, p);
+    return launch_pdl(
+        credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop, TIn>,
+        (unsigned)p.N, kThreads, 0, stream, p);
 }
 
-cudaError_t launch_forward(const Params &p_in, bool vec, cudaStream_t stream)
+template <typename TIn>
+cudaError_t launch_forward_typed(const Params &p_in, bool vec, cudaStream_t stream)
 {
     Params p = p_in;
     // decay^kItems in the kernel's multiply order, for the per-lane composite.
@@ -46,10 +48,20 @@ cudaError_t launch_forward(const Params &p_in, bool vec, cudaStream_t stream)
     for (int i = 1; i < kItems; ++i) p.beta_pow = p.gamma * p.beta_pow;
     const bool trunc = p.trunc != nullptr;
     if (vec)
-        return trunc ? launch_forward_variant<true, true>(p, stream)
-                     : launch_forward_variant<true, false>(p, stream);
-    return trunc ? launch_forward_variant<false, true>(p, stream)
-                 : launch_forward_variant<false, false>(p, stream);
+        return trunc ? launch_forward_variant<true, true, TIn>(p, stream)
+                     : launch_forward_variant<true, false, TIn>(p, stream);
+    return trunc ? launch_forward_variant<false, true, TIn>(p, stream)
+                 : launch_forward_variant<false, false, TIn>(p, stream);
+}
+
+cudaError_t launch_forward(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_forward_typed<float>(p, vec, stream);
+}
+
+cudaError_t launch_forward_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_forward_typed<uint16_t>(p, vec, stream);
 }
 
 }  // namespace rlca

@@ -7,4 +7,9 @@ cudaError_t launch_gae(const Params &p, bool vec, bool streamable, cudaStream_t 
 {
     return launch_estimator<Est::kGae>(p, vec, streamable, stream);
 }
+
+cudaError_t launch_gae_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator_bf16<Est::kGae>(p, vec, stream);
+}
 }  // namespace rlca

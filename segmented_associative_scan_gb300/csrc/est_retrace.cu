@@ -7,4 +7,9 @@ cudaError_t launch_retrace(const Params &p, bool vec, bool streamable, cudaStrea
 {
     return launch_estimator<Est::kRetrace>(p, vec, streamable, stream);
 }
+
+cudaError_t launch_retrace_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator_bf16<Est::kRetrace>(p, vec, stream);
+}
 }  // namespace rlca

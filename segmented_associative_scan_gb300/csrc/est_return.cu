@@ -7,4 +7,9 @@ cudaError_t launch_return(const Params &p, bool vec, bool streamable, cudaStream
 {
     return launch_estimator<Est::kReturn>(p, vec, streamable, stream);
 }
+
+cudaError_t launch_return_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator_bf16<Est::kReturn>(p, vec, stream);
+}
 }  // namespace rlca

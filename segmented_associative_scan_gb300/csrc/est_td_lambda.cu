@@ -7,6 +7,11 @@ cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStr
 {
     return launch_estimator<Est::kTdLambda>(p, vec, streamable, stream);
 }
+
+cudaError_t launch_td_lambda_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator_bf16<Est::kTdLambda>(p, vec, stream);
+}
 // Fused TD(lambda) for several lambdas: whole-row CTA tiles, or the row loop.
 template <bool VEC, bool TRUNC>
 cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)

@@ -7,4 +7,9 @@ cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream
 {
     return launch_estimator<Est::kVtrace>(p, vec, streamable, stream);
 }
+
+cudaError_t launch_vtrace_bf16(const Params &p, bool vec, cudaStream_t stream)
+{
+    return launch_estimator_bf16<Est::kVtrace>(p, vec, stream);
+}
 }  // namespace rlca

@@ -104,17 +104,26 @@ struct Chunk {
     unsigned valid;  // bit j: step t0+j exists in this row
 };
 
+// Row `off` of a per-step input array holding TIn elements (the Params pointers are
+// typed fp32; bf16 inputs are stored behind them as uint16_t bit patterns).
+template <typename TIn>
+__device__ __forceinline__ const TIn *in_row(const float *base, int64_t off)
+{
+    return reinterpret_cast<const TIn *>(base) + off;
+}
+
 // Successor of item ITEMS-1: the next lane's first item, or (lane 31) a direct load.
 // Every lane of the warp must call this (it shuffles).
-__device__ __forceinline__ float next_item(float first_item, const float *__restrict__ row,
+template <typename TIn = float>
+__device__ __forceinline__ float next_item(float first_item, const TIn *__restrict__ row,
                                            int t_next, bool need, int lane)
 {
     float s = __shfl_down_sync(kFullMask, first_item, 1);
-    if (lane == 31) s = need ? __ldg(row + t_next) : 0.f;
+    if (lane == 31) s = need ? InType<TIn>::cached(row + t_next) : 0.f;
     return need ? s : 0.f;
 }
 
-template <Est E, int ITEMS, bool VEC, bool TRUNC>
+template <Est E, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0, bool active,
                                            int lane, Chunk<ITEMS> &c)
 {
@@ -123,10 +132,10 @@ __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0,
     const int Te = active ? T : 0;  // an inactive thread sees an empty row
     const int64_t off = active ? row * p.ld : 0;
 
-    load_items<ITEMS, VEC>(p.reward + off, t0, Te, c.r);
-    if (Tr::kValue) load_items<ITEMS, VEC>(p.value + off, t0, Te, c.v);
-    if (Tr::kAux) load_items<ITEMS, VEC>(p.aux + off, t0, Te, c.x);
-    if (Tr::kRho) load_items<ITEMS, VEC>(p.rho + off, t0, Te, c.y);
+    load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, c.r);
+    if (Tr::kValue) load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.value, off), t0, Te, c.v);
+    if (Tr::kAux) load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.aux, off), t0, Te, c.x);
+    if (Tr::kRho) load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.rho, off), t0, Te, c.y);
     c.term = load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
     c.trunc = TRUNC ? load_flag_bits<ITEMS, VEC>(p.trunc + off, t0, Te) : 0u;
     c.valid = valid_items<ITEMS>(t0, Te);
@@ -135,9 +144,12 @@ __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0,
     c.stop = (c.term | c.trunc | window_end | ~c.valid) & all_items<ITEMS>();
 
     const bool need = active && (t0 + ITEMS < T);
-    if (Tr::kNextValue) c.v_next = next_item(c.v[0], p.value + off, t0 + ITEMS, need, lane);
-    if (Tr::kNextAux) c.x_next = next_item(c.x[0], p.aux + off, t0 + ITEMS, need, lane);
-    if (Tr::kNextRho) c.y_next = next_item(c.y[0], p.rho + off, t0 + ITEMS, need, lane);
+    if (Tr::kNextValue)
+        c.v_next = next_item<TIn>(c.v[0], in_row<TIn>(p.value, off), t0 + ITEMS, need, lane);
+    if (Tr::kNextAux)
+        c.x_next = next_item<TIn>(c.x[0], in_row<TIn>(p.aux, off), t0 + ITEMS, need, lane);
+    if (Tr::kNextRho)
+        c.y_next = next_item<TIn>(c.y[0], in_row<TIn>(p.rho, off), t0 + ITEMS, need, lane);
 }
 
 template <int ITEMS>
@@ -151,7 +163,7 @@ __device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next,
 // one picks beta or the reset marker. Successor values that need a load (truncated
 // steps and the window end) are fetched in a branch that few threads take.
 // V-trace keeps rho_t in c.x for the epilogue.
-template <Est E, int ITEMS>
+template <Est E, int ITEMS, typename TIn = float>
 __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chunk<ITEMS> &c,
                                       Affine (&e)[ITEMS])
 {
@@ -165,8 +177,9 @@ __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chun
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j)
             if (load_sv & (1u << j))
-                c.sv[j] = (c.trunc & (1u << j)) ? __ldg(p.trunc_value + off + t0 + j)
-                                                : (p.boot ? __ldg(p.boot + row) : 0.f);
+                c.sv[j] = (c.trunc & (1u << j))
+                              ? InType<TIn>::cached(in_row<TIn>(p.trunc_value, off) + t0 + j)
+                              : (p.boot ? __ldg(p.boot + row) : 0.f);
     }
 #pragma unroll
     for (int j = 0; j < ITEMS; ++j) {

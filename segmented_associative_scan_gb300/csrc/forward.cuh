@@ -23,7 +23,7 @@ namespace rlca {
 // One chunk: A at the step before the chunk is `carry_in`; `prev_ended` says whether the
 // step before lane 0's first step ended an episode. Returns A at the chunk's last step;
 // *last_ended gets whether that step ended an episode.
-template <int ITEMS, bool VEC, bool TRUNC>
+template <int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int t0, bool active,
                                                float carry_in, bool prev_ended,
                                                bool *last_ended)
@@ -34,7 +34,7 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
     const int64_t off = active ? row * p.ld : 0;
 
     float x[ITEMS];
-    load_items<ITEMS, VEC>(p.reward + off, t0, Te, x);
+    load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, x);
     const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
                                  : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
     const unsigned valid = valid_items<ITEMS>(t0, Te);
@@ -83,7 +83,7 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
     return affine_apply(whole, carry_in);
 }
 
-template <int ITEMS, bool VEC, bool TRUNC, int WARPS = 4>
+template <int ITEMS, bool VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
 __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params p)
 {
     grid_dependency_sync();
@@ -96,14 +96,14 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
         const int chunk = lane - local_row * p.chunks_per_row;
         const int64_t row = job * p.rows_per_tile + local_row;
         const bool active = local_row < p.rows_per_tile && row < p.N;
-        forward_chunk<ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f, false,
-                                         &last_ended);
+        forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f, false,
+                                              &last_ended);
     } else {
         if (job >= p.N) return;  // the whole warp leaves together
         float carry = 0.f;
         for (int s = 0; s < p.segs; ++s)
-            carry = forward_chunk<ITEMS, VEC, TRUNC>(p, job, s * CH + lane * ITEMS, true,
-                                                     carry, last_ended, &last_ended);
+            carry = forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, job, s * CH + lane * ITEMS, true,
+                                                          carry, last_ended, &last_ended);
     }
 }
 
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
 // belongs to the previous warp, so the warp scans as if it did not, and the flag is
 // applied after the exchange instead: the warp's carry-in becomes 0 (its first step then
 // equals x exactly) and its total is marked as a reset for the warps after it.
-template <int NT, int ITEMS, bool VEC, bool TRUNC>
+template <int NT, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int t0, bool active,
                                               float carry_in, bool prev_ended, bool *last_ended,
                                               ScanSmem<NT> &sm, int buf)
@@ -131,7 +131,7 @@ __device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int 
     const int64_t off = active ? row * p.ld : 0;
 
     float x[ITEMS];
-    load_items<ITEMS, VEC>(p.reward + off, t0, Te, x);
+    load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, x);
     const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
                                  : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
     const unsigned valid = valid_items<ITEMS>(t0, Te);
@@ -197,7 +197,7 @@ __device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int 
 
 // CTA-tiled forward scan: T <= NT * ITEMS packs whole rows into a tile; longer rows are
 // walked tile by tile from the first, with the carry in registers.
-template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
+template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, typename TIn = float>
 __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
@@ -209,15 +209,16 @@ __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
         const int64_t row = (int64_t)blockIdx.x * p.rows_per_tile + local_row;
         const bool active = local_row < p.rows_per_tile && row < p.N;
         bool last_ended = false;
-        forward_tile<NT, ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f, false,
-                                            &last_ended, sm, 0);
+        forward_tile<NT, ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f, false,
+                                                 &last_ended, sm, 0);
     } else {
         const int64_t row = blockIdx.x;
         float carry = 0.f;
         bool ended = false;
         for (int s = 0; s < p.segs; ++s)
-            carry = forward_tile<NT, ITEMS, VEC, TRUNC>(p, row, s * TILE + threadIdx.x * ITEMS,
-                                                        true, carry, ended, &ended, sm, s & 1);
+            carry = forward_tile<NT, ITEMS, VEC, TRUNC, TIn>(p, row,
+                                                             s * TILE + threadIdx.x * ITEMS, true,
+                                                             carry, ended, &ended, sm, s & 1);
     }
 }
 

@@ -145,7 +145,7 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
 // Scan the loaded steps this thread owns, write the outputs and return A at the tile's
 // first step. The tile's carry-in (A at the step after the tile) is `carry_in`, or,
 // with LB, the result of the look-back (`epoch` and `seg` identify the tile's state).
-template <Est E, int NT, int ITEMS, bool VEC, bool LB>
+template <Est E, int NT, int ITEMS, bool VEC, bool LB, typename TIn = float>
 __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, int64_t row,
                                             int t0, float carry_in, ScanSmem<NT> &sm, int buf,
                                             int seg = 0, unsigned epoch = 0)
@@ -155,7 +155,7 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
     const int warp = threadIdx.x >> 5;
 
     Affine e[ITEMS];
-    build<E, ITEMS>(p, row, t0, c, e);
+    build<E, ITEMS, TIn>(p, row, t0, c, e);
 
     // Thread aggregate: e_0 (+) e_1 (+) ... (+) e_{ITEMS-1}.
     const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
@@ -207,14 +207,14 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
 }
 
 // Load this thread's steps from global memory, then scan_chunk.
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB>
+template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB, typename TIn = float>
 __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
                                            float carry_in, ScanSmem<NT> &sm, int buf,
                                            int seg = 0, unsigned epoch = 0)
 {
     Chunk<ITEMS> c;
-    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, threadIdx.x & 31, c);
-    return scan_chunk<E, NT, ITEMS, VEC, LB>(p, c, row, t0, carry_in, sm, buf, seg, epoch);
+    load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, t0, active, threadIdx.x & 31, c);
+    return scan_chunk<E, NT, ITEMS, VEC, LB, TIn>(p, c, row, t0, carry_in, sm, buf, seg, epoch);
 }
 
 // Programmatic dependent launch: wait until the previous kernel in the stream has
@@ -227,7 +227,8 @@ __device__ __forceinline__ void grid_dependency_sync()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, int MINB = 1>
+template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, int MINB = 1,
+          typename TIn = float>
 __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
@@ -238,12 +239,13 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
         const int chunk = threadIdx.x - local_row * p.chunks_per_row;
         const int64_t row = (int64_t)blockIdx.x * p.rows_per_tile + local_row;
         const bool active = local_row < p.rows_per_tile && row < p.N;
-        scan_tile<E, NT, ITEMS, VEC, TRUNC, false>(p, row, chunk * ITEMS, active, 0.f, sm, 0);
+        scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn>(p, row, chunk * ITEMS, active, 0.f, sm,
+                                                        0);
     } else if (TL == Tiling::kRowLoop) {
         const int64_t row = blockIdx.x;
         float carry = 0.f;
         for (int s = p.segs - 1; s >= 0; --s)
-            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false>(
+            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn>(
                 p, row, s * TILE + threadIdx.x * ITEMS, true, carry, sm, s & 1);
     } else {
         LookbackHeader *h = static_cast<LookbackHeader *>(p.ws);
@@ -258,8 +260,8 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
         const unsigned epoch = sm.epoch;
         const int64_t row = vid / (unsigned)p.segs;
         const int seg = p.segs - 1 - (int)(vid - row * p.segs);
-        scan_tile<E, NT, ITEMS, VEC, TRUNC, true>(p, row, seg * TILE + threadIdx.x * ITEMS,
-                                                  true, 0.f, sm, 0, seg, epoch);
+        scan_tile<E, NT, ITEMS, VEC, TRUNC, true, TIn>(p, row, seg * TILE + threadIdx.x * ITEMS,
+                                                       true, 0.f, sm, 0, seg, epoch);
         // The last CTA to finish rearms the workspace for the next launch.
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -322,15 +324,15 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
 // aggregates, a warp suffix scan, and the chunk's carry-in (A at the step after the
 // chunk) applied directly. Returns A at the chunk's first step.
-template <Est E, int ITEMS, bool VEC, bool TRUNC>
+template <Est E, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0, bool active,
                                             float carry_in)
 {
     const int lane = threadIdx.x & 31;
     Chunk<ITEMS> c;
-    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
+    load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, t0, active, lane, c);
     Affine e[ITEMS];
-    build<E, ITEMS>(p, row, t0, c, e);
+    build<E, ITEMS, TIn>(p, row, t0, c, e);
     const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
     const Affine incl = warp_suffix_scan(agg, lane);
     Affine excl = shfl_down(incl, 1);
@@ -349,7 +351,7 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
 //   first with the carry in a register.
 // All warps of a typical launch are resident at once, so each keeps its next chunk's
 // loads in flight without any cross-warp wait.
-template <Est E, int ITEMS, bool VEC, bool TRUNC, int WARPS = 4>
+template <Est E, int ITEMS, bool VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
 __global__ void __launch_bounds__(32 * WARPS) credit_warp_kernel(const Params p)
 {
     grid_dependency_sync();
@@ -361,12 +363,13 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_kernel(const Params p)
         const int chunk = lane - local_row * p.chunks_per_row;
         const int64_t row = job * p.rows_per_tile + local_row;
         const bool active = local_row < p.rows_per_tile && row < p.N;
-        warp_chunk<E, ITEMS, VEC, TRUNC>(p, row, chunk * ITEMS, active, 0.f);
+        warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f);
     } else {
         if (job >= p.N) return;  // the whole warp leaves together
         float carry = 0.f;
         for (int s = p.segs - 1; s >= 0; --s)
-            carry = warp_chunk<E, ITEMS, VEC, TRUNC>(p, job, s * CH + lane * ITEMS, true, carry);
+            carry = warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, job, s * CH + lane * ITEMS, true,
+                                                          carry);
     }
 }
 

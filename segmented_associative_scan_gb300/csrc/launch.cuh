@@ -8,6 +8,7 @@
 #pragma once
 
 #include <atomic>
+#include <type_traits>
 
 #include "kernels.cuh"
 #include "warp_stream.cuh"
@@ -76,7 +77,7 @@ inline Path choose_path(int64_t N, int T, bool vec, bool streamable, bool lookba
 
 // ------------------------------------------------------------------ CTA tile paths
 
-template <Est E, bool VEC, bool TRUNC>
+template <Est E, bool VEC, bool TRUNC, typename TIn = float>
 cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 {
     if (path == Path::kCtaRows) {
@@ -85,41 +86,43 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
         p.rows_per_tile = kTile / t_pad;
         p.segs = 1;
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
-        return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows>,
-                          grid, kThreads, 0, stream, p);
+        return launch_pdl(
+            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows, 1, TIn>, grid,
+            kThreads, 0, stream, p);
     }
     p.chunks_per_row = kTile / kItems;
     p.rows_per_tile = 1;
     p.segs = (p.T + kTile - 1) / kTile;
     if (path == Path::kLookback)
         return launch_pdl(
-            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback>,
+            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback, 1, TIn>,
             (unsigned)(p.N * p.segs), kThreads, 0, stream, p);
-    return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop>,
-                      (unsigned)p.N, kThreads, 0, stream, p);
+    return launch_pdl(
+        credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop, 1, TIn>,
+        (unsigned)p.N, kThreads, 0, stream, p);
 }
 
 // ------------------------------------------------------------------ warp paths
 
-template <Est E, bool VEC, bool TRUNC>
+template <Est E, bool VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
 cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 {
-    constexpr int CH = 32 * kItems;
+    constexpr int CH = 32 * ITEMS;
     int64_t jobs;
     if (p.T <= CH) {
-        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        const int t_pad = (p.T + ITEMS - 1) / ITEMS * ITEMS;
         p.segs = 1;
-        p.chunks_per_row = t_pad / kItems;
+        p.chunks_per_row = t_pad / ITEMS;
         p.rows_per_tile = CH / t_pad;
         jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
     } else {
         p.segs = (p.T + CH - 1) / CH;
-        p.chunks_per_row = CH / kItems;
+        p.chunks_per_row = CH / ITEMS;
         p.rows_per_tile = 1;
         jobs = p.N;
     }
     const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(credit_warp_kernel<E, kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+    return launch_pdl(credit_warp_kernel<E, ITEMS, VEC, TRUNC, kWarpsPerCta, TIn>, grid,
                       32 * kWarpsPerCta, 0, stream, p);
 }
 
@@ -179,17 +182,57 @@ cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
     return launch_cta<E, VEC, TRUNC>(p, path, stream);
 }
 
+// beta^kItems in the order the kernels multiply (b = beta * b), for the constant-beta
+// estimators' per-thread composite.
+template <Est E>
+void set_beta_pow(Params &p)
+{
+    const float beta = E == Est::kReturn ? p.gamma : p.gamma_lambda;
+    p.beta_pow = beta;
+    for (int i = 1; i < kItems; ++i) p.beta_pow = beta * p.beta_pow;
+}
+
+// bf16 per-step inputs (uint16_t bit patterns, fp32 arithmetic): warp-owned rows up to
+// one warp chunk, CTA tiles (whole rows or the row loop) beyond; GAE rows longer than a
+// warp chunk go to warp-owned rows with 16 steps per lane (measured fastest for bf16).
+template <Est E>
+cudaError_t launch_estimator_bf16(const Params &p_in, bool vec, cudaStream_t stream)
+{
+    Params p = p_in;
+    set_beta_pow<E>(p);
+    if (E == Est::kGae && p.T > 32 * kItems) {
+        // 16 steps per lane: beta^16 for the per-lane composite.
+        p.beta_pow = p.gamma_lambda;
+        for (int i = 1; i < 16; ++i) p.beta_pow = p.gamma_lambda * p.beta_pow;
+        const bool trunc = p.trunc != nullptr;
+        if (vec)
+            return trunc ? launch_warp_rows<E, true, true, uint16_t, 16>(p, stream)
+                         : launch_warp_rows<E, true, false, uint16_t, 16>(p, stream);
+        return trunc ? launch_warp_rows<E, false, true, uint16_t, 16>(p, stream)
+                     : launch_warp_rows<E, false, false, uint16_t, 16>(p, stream);
+    }
+    const bool trunc = p.trunc != nullptr;
+    const Path path = p.T <= 32 * kItems ? Path::kWarpRows
+                                         : (p.T > kTile ? Path::kCtaRowLoop : Path::kCtaRows);
+    auto go = [&](auto vec_tag, auto trunc_tag) {
+        constexpr bool V = decltype(vec_tag)::value;
+        constexpr bool R = decltype(trunc_tag)::value;
+        if (path == Path::kWarpRows) return launch_warp_rows<E, V, R, uint16_t>(p, stream);
+        return launch_cta<E, V, R, uint16_t>(p, path, stream);
+    };
+    using T_ = std::true_type;
+    using F_ = std::false_type;
+    if (vec) return trunc ? go(T_{}, T_{}) : go(T_{}, F_{});
+    return trunc ? go(F_{}, T_{}) : go(F_{}, F_{});
+}
+
 // Launch one estimator; `vec` = 16-byte aligned rows (128-bit access), `streamable` =
 // layout fit for 16-byte bulk copies (see api.cu).
 template <Est E>
 cudaError_t launch_estimator(const Params &p_in, bool vec, bool streamable, cudaStream_t stream)
 {
     Params p = p_in;
-    // beta^kItems in the order the kernels multiply (b = beta * b), for the constant-beta
-    // estimators' per-thread composite.
-    const float beta = E == Est::kReturn ? p.gamma : p.gamma_lambda;
-    p.beta_pow = beta;
-    for (int i = 1; i < kItems; ++i) p.beta_pow = beta * p.beta_pow;
+    set_beta_pow<E>(p);
     const Path path = choose_path<E>(p.N, p.T, vec, streamable, p.ws != nullptr);
     const bool trunc = p.trunc != nullptr;
     if (path == Path::kWarpStream)
@@ -208,9 +251,16 @@ cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStr
 cudaError_t launch_gae(const Params &p, bool vec, bool streamable, cudaStream_t stream);
 cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
 cudaError_t launch_retrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+// The same with bf16 per-step inputs.
+cudaError_t launch_return_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_td_lambda_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_gae_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_vtrace_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_retrace_bf16(const Params &p, bool vec, cudaStream_t stream);
 // Fused TD(lambda) for p.multi.count lambdas (outputs in p.multi.out).
 cudaError_t launch_td_multi(const Params &p, bool vec, cudaStream_t stream);
 // Forward scans: p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
 cudaError_t launch_forward(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_forward_bf16(const Params &p, bool vec, cudaStream_t stream);
 
 }  // namespace rlca

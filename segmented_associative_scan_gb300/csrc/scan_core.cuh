@@ -88,23 +88,73 @@ __device__ __forceinline__ unsigned valid_items(int t0, int T)
     return n >= ITEMS ? all_items<ITEMS>() : (n > 0 ? (1u << n) - 1u : 0u);
 }
 
-// ITEMS consecutive floats of one row starting at column t0; columns >= T read as 0.
-template <int ITEMS, bool VEC>
-__device__ __forceinline__ void load_items(const float *__restrict__ row, int t0, int T,
+// ------------------------------------------------------------- input element types
+
+// Per-step inputs are fp32 or bf16 (`uint16_t` holding the bf16 bit pattern); the
+// arithmetic is fp32 either way. A bf16 value widens to fp32 exactly (its bits are the
+// high half of the fp32 pattern). `kPerVec` elements fill one 128-bit load.
+template <typename TIn>
+struct InType;
+
+template <>
+struct InType<float> {
+    static constexpr int kPerVec = 4;
+    __device__ static __forceinline__ float stream(const float *p) { return __ldcs(p); }
+    __device__ static __forceinline__ float cached(const float *p) { return __ldg(p); }
+    __device__ static __forceinline__ void unpack(const uint4 &q, float *x)
+    {
+        x[0] = __uint_as_float(q.x);
+        x[1] = __uint_as_float(q.y);
+        x[2] = __uint_as_float(q.z);
+        x[3] = __uint_as_float(q.w);
+    }
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits)
+{
+    return __uint_as_float(bits << 16);
+}
+
+template <>
+struct InType<uint16_t> {
+    static constexpr int kPerVec = 8;
+    __device__ static __forceinline__ float stream(const uint16_t *p)
+    {
+        return bf16_bits_to_float(__ldcs(reinterpret_cast<const unsigned short *>(p)));
+    }
+    __device__ static __forceinline__ float cached(const uint16_t *p)
+    {
+        return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
+    __device__ static __forceinline__ void unpack(const uint4 &q, float *x)
+    {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// ITEMS consecutive inputs of one row starting at column t0, widened to fp32; columns
+// >= T read as 0. VEC: 128-bit loads (the row start and t0 are 16-byte aligned).
+template <int ITEMS, bool VEC, typename TIn = float>
+__device__ __forceinline__ void load_items(const TIn *__restrict__ row, int t0, int T,
                                            float (&x)[ITEMS])
 {
+    constexpr int PV = InType<TIn>::kPerVec;
+    static_assert(ITEMS % PV == 0, "a thread's items fill whole 128-bit loads");
     if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
-        for (int k = 0; k < ITEMS / 4; ++k) {
-            const float4 q = ld_stream(reinterpret_cast<const float4 *>(row + t0) + k);
-            x[4 * k + 0] = q.x;
-            x[4 * k + 1] = q.y;
-            x[4 * k + 2] = q.z;
-            x[4 * k + 3] = q.w;
+        for (int k = 0; k < ITEMS / PV; ++k) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(row + t0) + k);
+            InType<TIn>::unpack(q, x + PV * k);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < ITEMS; ++j) x[j] = (t0 + j < T) ? ld_stream(row + t0 + j) : 0.f;
+        for (int j = 0; j < ITEMS; ++j)
+            x[j] = (t0 + j < T) ? InType<TIn>::stream(row + t0 + j) : 0.f;
     }
 }
 

@@ -72,16 +72,18 @@ class Placed:
 
 
 def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0",
-            check_guards=True, drop_second_output=False, workspace=None):
+            check_guards=True, drop_second_output=False, workspace=None,
+            in_dtype=torch.float32):
     """Run `est` on the CUDA path; returns {output name: float64 array}. `workspace`
-    (a zeroed uint8 CUDA tensor) selects the look-back (_ex) entry point."""
+    (a zeroed uint8 CUDA tensor) selects the look-back (_ex) entry point; in_dtype
+    torch.bfloat16 places the data inputs as bf16 (the _bf16 entry points)."""
     N, T = ro.N, ro.T
     ws = dict(workspace=workspace)
     ld = T if ld is None else ld
     p = dict(DEFAULT_PARAMS[est], **params)
 
     def f32(a):
-        return None if a is None else Placed(a, N, T, ld, offset, torch.float32, 0.0, device)
+        return None if a is None else Placed(a, N, T, ld, offset, in_dtype, 0.0, device)
 
     def flag(a):
         if a is None:
@@ -141,3 +143,16 @@ def assert_parity(gpu: dict, ref: dict, what: str, tol=TOL):
         err = np.max(np.abs(g[ok] - r[ok]))
         bound = tol * (1.0 + np.max(np.abs(r[ok])))
         assert err <= bound, f"{what}/{name}: max|err| {err:.3e} > {bound:.3e}"
+
+
+def bf16_rounded(ro):
+    """The rollout with every per-step data input rounded to bf16 (kept as fp32 arrays,
+    so the oracle sees exactly the values the bf16 kernels widen)."""
+    import copy
+    out = copy.copy(ro)
+    for k in ("reward", "value", "trunc_value", "log_rho", "q_taken", "expected_q", "rho"):
+        a = getattr(ro, k)
+        if a is not None:
+            setattr(out, k, torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+                    .to(torch.float32).numpy())
+    return out
