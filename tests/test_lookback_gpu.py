@@ -1,7 +1,8 @@
-"""GPU parity of the look-back path (_ex entry points with a caller workspace): every
-tile of every row runs in its own CTA and finds its carry-in from the later tiles of
-its row. Same oracle and tolerance as the other parity tests; the bounded wait is
-exercised by a testing entry point that makes every tile withhold its state."""
+"""GPU parity of the look-back path (_ex entry points with a caller workspace, rows too
+few to fill the GPU): every tile of every row runs in its own CTA and finds its
+carry-in from the later tiles of its row. Same oracle and tolerance as the other parity
+tests; the bounded wait is exercised by a testing entry point that makes every tile
+withhold its state."""
 import ctypes
 
 import numpy as np
@@ -43,13 +44,50 @@ def test_lookback_long_episodes_cross_many_tiles():
                       run_oracle(est, ro, dict(gamma=0.999, lam=0.999)), f"{est} long")
 
 
-def test_lookback_workload_retrace_2048x4096():
+def _epoch(ws):
+    """Launches that used the workspace's look-back state (the header's first word)."""
+    return int(ws[:4].cpu().view(torch.int32)[0])
+
+
+def test_lookback_only_when_rows_cannot_fill_the_gpu():
+    """With a workspace, look-back runs below two rows per SM and leaves the workspace
+    untouched from there on (the row loop is faster once the rows fill the GPU)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 2049
+    for N, uses in ((2 * sms - 1, True), (2 * sms, False)):
+        ro = sr.generic(N, T, seed=N, p_term=0.002, p_trunc=0.001)
+        ws = rlca.make_workspace(N, T)
+        ws.zero_()
+        for i, est in enumerate(ESTIMATORS):
+            assert_parity(run_gpu(est, ro, {}, workspace=ws), run_oracle(est, ro, {}),
+                          f"{est} N={N} T={T}")
+            assert _epoch(ws) == (i + 1 if uses else 0), (N, est)
+        assert rlca.workspace_check(ws) == 0
+
+
+@pytest.mark.parametrize("est", ["return", "gae"])
+def test_very_long_rows(est):
+    """Two rows of 2^20 + 7 steps (1025 tiles each, the last ragged): the look-back and
+    the row loop over the whole row, with episodes that span hundreds of tiles."""
+    N, T = 2, (1 << 20) + 7
+    ro = sr.generic(N, T, seed=21, p_term=2e-6, p_trunc=1e-6)
+    p = dict(gamma=0.999, lam=0.99)
+    ref = run_oracle(est, ro, p)
+    ws = rlca.make_workspace(N, T)
+    assert_parity(run_gpu(est, ro, p, workspace=ws), ref, f"{est} look-back T={T}")
+    assert _epoch(ws) == 1 and rlca.workspace_check(ws) == 0
+    assert_parity(run_gpu(est, ro, p), ref, f"{est} row loop T={T}")
+
+
+def test_ex_workload_retrace_2048x4096():
+    """The retrace workload through the _ex call: 2048 rows fill the GPU, so the row
+    loop runs and the workspace stays as it was, call after call."""
     ro = sr.retrace()
     p = dict(gamma=ro.params["gamma"], lam=ro.params["lam"])
     ws = rlca.make_workspace(ro.N, ro.T)
     ref = run_oracle("retrace", ro, p)
-    for _ in range(3):  # the workspace is reused: each launch rearms it for the next
-        assert_parity(run_gpu("retrace", ro, p, workspace=ws), ref, "retrace look-back")
+    for _ in range(3):
+        assert_parity(run_gpu("retrace", ro, p, workspace=ws), ref, "retrace _ex")
     assert rlca.workspace_check(ws) == 0
 
 
