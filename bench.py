@@ -48,27 +48,44 @@ WORKLOADS = {
     "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
     "prefix_sum": "episodic prefix sum (forward scan), fp32, num_envs=4096, seq_len=1024",
 }
-KERNELS = {
-    "gae": "credit_warp_stream_kernel<GAE> (warp-owned rows, per-warp TMA ring)",
-    "return": "credit_scan_kernel<return, whole-row CTA tiles>",
-    "td_lambda": "credit_scan_kernel<TD(lambda), whole-row CTA tiles>",
-    "vtrace": "credit_scan_kernel<V-trace, whole-row CTA tiles>",
-    "retrace": "credit_scan_kernel<Retrace, whole-row CTA tiles>",
-    "td_multi": "credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)",
-    "gae_bf16": "credit_scan_kernel<GAE, bf16 inputs, whole-row CTA tiles>",
-    "trace": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
-    "prefix_sum": "credit_forward_tile_kernel (whole-row CTA tiles, forward)",
-}
+_EST_NAME = {"gae": "GAE", "gae_bf16": "GAE, bf16 inputs", "return": "return",
+             "td_lambda": "TD(lambda)", "vtrace": "V-trace", "retrace": "Retrace"}
+
+
+def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
+    """The kernel the library's dispatch picks for this call (contiguous rows)."""
+    if est in ("trace", "prefix_sum"):
+        if T <= 256:
+            return "credit_forward_kernel (warp-owned rows, forward)"
+        return ("credit_forward_tile_kernel (whole-row CTA tiles, forward)" if T <= 1024
+                else "credit_forward_tile_kernel (CTA row loop, forward)")
+    if est == "td_multi":
+        return ("credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)" if T <= 1024
+                else "credit_td_multi_kernel (CTA row loop, 3 lambdas per load)")
+    name = _EST_NAME[est]
+    if est == "gae_bf16":
+        return (f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)" if T <= 256
+                else f"credit_warp_kernel<{name}> (warp-owned rows, 16 steps/lane)")
+    if T > 1024:
+        if workspace and N < 2 * sms:
+            return f"credit_scan_kernel<{name}, look-back across CTA tiles>"
+        return f"credit_scan_kernel<{name}, CTA row loop>"
+    if T <= 256:
+        return f"credit_warp_kernel<{name}> (warp-owned rows)"
+    if est == "gae" and T % 16 == 0:
+        return f"credit_warp_stream_kernel<{name}> (warp-owned rows, per-warp TMA ring)"
+    if est == "gae":
+        return f"credit_warp_kernel<{name}> (warp-owned rows)"
+    return f"credit_scan_kernel<{name}, whole-row CTA tiles>"
+
+
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM bytes per launch measured by ncu for the GAE [4096,1024] kernel, keyed by a hash of
-# the kernel sources at the time of the capture; null once the kernels change.
-NCU_TRAFFIC = {
-    # credit_warp_stream_kernel<GAE>: dram read 43.01 MB + write 1.13 MB in one captured
-    # launch (the outputs stay in L2 within it): profiles/gae_trunc_4096x1024_kernel.md
-    "152a3feb6fd0aaad": 44_138_240,
-}
+# DRAM bytes (read + write) per launch measured by ncu, keyed by (hash of the kernel
+# sources at the time of the capture, estimator, N, T, workspace); null once the kernels
+# change. Filled from the ncu summaries under profiles/.
+NCU_TRAFFIC: dict = {}
 
 
 def kernel_source_hash() -> str:
@@ -233,6 +250,7 @@ class DeviceSet:
             t(ro.log_rho), t(ro.q_taken), t(ro.expected_q), t(ro.rho))
         z = lambda: torch.empty((ro.N, ro.T), dtype=torch.float32, device=device)
         self.out0, self.out1, self.out2 = z(), z(), z()
+        self.ws = None  # look-back workspace (the _ex entry points), when asked for
 
     def clone(self):
         import torch
@@ -246,23 +264,25 @@ def launch(rlca, est, s, params):
     fl = dict(terminated=s.terminated, truncated=s.truncated,
               trunc_value=s.trunc_value if s.truncated is not None else None)
     g = params["gamma"]
+    ws = s.ws
     if est in ("gae", "gae_bf16"):
         rlca.rlca_gae(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
-                      lam=params["lam"], advantages=s.out0, returns=s.out1)
+                      lam=params["lam"], advantages=s.out0, returns=s.out1, workspace=ws)
     elif est == "return":
         rlca.rlca_discounted_return(s.reward, **fl, bootstrap=s.bootstrap, gamma=g,
-                                    returns=s.out0)
+                                    returns=s.out0, workspace=ws)
     elif est == "td_lambda":
         rlca.rlca_td_lambda(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
-                            lam=params["lam"], targets=s.out0)
+                            lam=params["lam"], targets=s.out0, workspace=ws)
     elif est == "vtrace":
         rlca.rlca_vtrace(s.reward, s.value, s.log_rho, **fl, bootstrap=s.bootstrap, gamma=g,
                          lam=params["lam"], rho_bar=params["rho_bar"],
                          c_bar=params["c_bar"], pg_rho_bar=params["pg_rho_bar"],
-                         vs=s.out0, pg_advantages=s.out1)
+                         vs=s.out0, pg_advantages=s.out1, workspace=ws)
     elif est == "retrace":
         rlca.rlca_retrace(s.reward, s.q_taken, s.expected_q, s.rho, **fl,
-                          bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0)
+                          bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0,
+                          workspace=ws)
     elif est == "td_multi":
         rlca.rlca_td_lambda_multi(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
                                   lams=params["lams"], targets=[s.out0, s.out1, s.out2])
@@ -409,9 +429,13 @@ def gpu_arm(args, rank, world, local_rank, dist):
     ro0 = workload_inputs(est, N, T, seed=1000 * rank)
     nbytes = algorithmic_bytes(est, ro0)
     n_sets = n_sets_for(nbytes)
-    sets = [DeviceSet(ro0, device)]
+    data_dtype = torch.bfloat16 if est.endswith("_bf16") else None
+    sets = [DeviceSet(ro0, device, data_dtype)]
     for i in range(1, n_sets):
-        sets.append(DeviceSet(workload_inputs(est, N, T, 1000 * rank + i), device))
+        sets.append(DeviceSet(workload_inputs(est, N, T, 1000 * rank + i), device, data_dtype))
+    if args.workspace:
+        for s in sets:
+            s.ws = rlca.make_workspace(N, T, device)
     params = est_params(est, ro0)
     step_bytes = [algorithmic_bytes(est, s.ro) for s in sets]
 
@@ -454,7 +478,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     achieved = kernel_bytes_per_step / (launch_us * 1e-6) / 1e9
     value = job_throughput(world, N, T, K, ms_max)
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(src_hash)
+    traffic = NCU_TRAFFIC.get((src_hash, est, N, T, bool(args.workspace)))
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 6),
@@ -465,6 +489,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
             else f"{est}, fp32, num_envs={N}, seq_len={T}", "estimator": est, "num_envs": N,
             "seq_len": T, "gamma": params["gamma"], "lambda": params.get("lam"),
             "input_sets": n_sets,
+            "entry": "_ex entry point with a caller workspace" if args.workspace
+                     else "plain entry point",
             "l2": (f"inputs larger than L2: {n_sets} distinct batches of "
                    f"{nbytes / 1e6:.1f} MB rotate ({n_sets * nbytes / 1e6:.0f} MB > "
                    f"{L2_BYTES / 1e6:.0f} MB L2)") if n_sets * nbytes > L2_BYTES else
@@ -475,7 +501,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": KERNELS[est],
+            "kernel": kernel_desc(est, N, T, args.workspace,
+                                  torch.cuda.get_device_properties(device).multi_processor_count),
             "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),
             "launch_us": round(launch_us, 3), "peak_source": peak_src,
             "frac_of_8tbs": round(achieved / 8000.0, 4), "kernel_source": src_hash},
@@ -550,6 +577,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--workspace", action="store_true",
+                    help="give every call a look-back workspace (the _ex entry points of the "
+                         "five reverse estimators)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-estimators", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -561,6 +591,9 @@ def main():
         args.cpu_seconds = 0.0
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
+    if args.workspace and args.estimator not in ("gae", "return", "td_lambda", "vtrace",
+                                                 "retrace"):
+        ap.error("--workspace applies to the five fp32 reverse estimators")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

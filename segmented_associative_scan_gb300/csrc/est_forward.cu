@@ -27,6 +27,10 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         p.chunks_per_row = t_pad / kItems;
         p.rows_per_tile = kTile / t_pad;
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        if (p.rows_per_tile == 1)
+            return launch_pdl(
+                credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRow, TIn>,
+                grid, kThreads, 0, stream, p);
         return launch_pdl(
             credit_forward_tile_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows, TIn>, grid,
             kThreads, 0, stream, p);

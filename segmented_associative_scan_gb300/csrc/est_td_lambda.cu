@@ -22,6 +22,9 @@ cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
         p.rows_per_tile = kTile / t_pad;
         p.segs = 1;
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        if (p.rows_per_tile == 1)
+            return launch_pdl(credit_td_multi_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRow>,
+                              grid, kThreads, 0, stream, p);
         return launch_pdl(credit_td_multi_kernel<kThreads, kItems, VEC, TRUNC, Tiling::kRows>,
                           grid, kThreads, 0, stream, p);
     }

@@ -211,6 +211,10 @@ __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
         bool last_ended = false;
         forward_tile<NT, ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f, false,
                                                  &last_ended, sm, 0);
+    } else if (TL == Tiling::kRow) {
+        bool last_ended = false;
+        forward_tile<NT, ITEMS, VEC, TRUNC, TIn>(p, blockIdx.x, threadIdx.x * ITEMS, true, 0.f,
+                                                 false, &last_ended, sm, 0);
     } else {
         const int64_t row = blockIdx.x;
         float carry = 0.f;

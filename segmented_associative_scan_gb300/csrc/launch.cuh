@@ -81,19 +81,20 @@ inline int sm_count()
 // look-back is 1.9x faster, at [512, 16384] 1.1x slower, at [2048, 4096] 1.3x slower).
 inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 
-// Measured on GB300 (see the design notes): rows of at most one warp chunk (256 steps)
-// go to warp-owned rows, which need no CTA barrier; up to one CTA tile (1024 steps) the
-// CTA tile kernel, which loads a whole row at once, wins for every estimator but GAE,
-// whose extra flag stream makes the barrier-free warp-streaming kernel faster; longer
-// rows loop over CTA tiles (or use look-back with a workspace).
+// Measured on GB300 (CUDA-event timing, inputs rotated past L2): rows of at most one
+// warp chunk (256 steps) go to warp-owned rows, which need no CTA barrier; up to one CTA
+// tile (1024 steps) the CTA tile kernel, which loads a whole row at once, wins for every
+// estimator but GAE with truncation: there the dependent load of the truncation values
+// stalls a whole CTA, and the barrier-free warp-streaming kernel is 8% faster (14.7 vs
+// 16.1 us at [4096, 1024]); without truncation the CTA kernel is 6% faster (12.7 vs
+// 13.5 us). Longer rows loop over CTA tiles (or use look-back with a workspace).
 template <Est E>
-inline Path choose_path(int64_t N, int T, bool vec, bool streamable, bool lookback)
+inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool trunc)
 {
     if (T > kTile) return lookback && lookback_pays(N) ? Path::kLookback : Path::kCtaRowLoop;
     if (T <= 32 * kItems) return Path::kWarpRows;
-    if (E == Est::kGae) return streamable ? Path::kWarpStream : Path::kWarpRows;
-    (void)N;
-    (void)vec;
+    if (E == Est::kGae && (trunc || 2 * T <= kTile))
+        return streamable ? Path::kWarpStream : Path::kWarpRows;
     return Path::kCtaRows;
 }
 
@@ -108,6 +109,10 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
         p.rows_per_tile = kTile / t_pad;
         p.segs = 1;
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
+        if (p.rows_per_tile == 1)
+            return launch_pdl(
+                credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRow, 1, TIn>, grid,
+                kThreads, 0, stream, p);
         return launch_pdl(
             credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows, 1, TIn>, grid,
             kThreads, 0, stream, p);
@@ -254,8 +259,8 @@ cudaError_t launch_estimator(const Params &p_in, bool vec, bool streamable, cuda
 {
     Params p = p_in;
     set_beta_pow<E>(p);
-    const Path path = choose_path<E>(p.N, p.T, vec, streamable, p.ws != nullptr);
     const bool trunc = p.trunc != nullptr;
+    const Path path = choose_path<E>(p.N, p.T, streamable, p.ws != nullptr, trunc);
     if (path == Path::kWarpStream)
         return trunc ? launch_warp_stream<E, true>(p, stream)
                      : launch_warp_stream<E, false>(p, stream);

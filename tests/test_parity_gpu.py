@@ -159,6 +159,19 @@ def test_row_stride_and_alignment(ld_extra, offset, T):
         assert_parity(g, run_oracle(est, ro, {}), f"{est} ld=T+{ld_extra} off={offset}")
 
 
+@pytest.mark.parametrize("ld_extra,offset", [(0, 0), (4, 0), (3, 0), (0, 1)])
+@pytest.mark.parametrize("T", [257, 300, 512, 513, 777, 1023, 1024])
+def test_without_truncation(ld_extra, offset, T):
+    """No truncation tensor at all: GAE rows longer than half a tile then take the CTA
+    kernel (one row per CTA) instead of the warp-streaming kernel."""
+    ro = sr.generic(37, T, seed=90 + T, p_term=0.01, p_trunc=0.0)
+    ro.truncated = None
+    for est in ESTIMATORS:
+        g = run_gpu(est, ro, {}, ld=T + ld_extra, offset=offset)
+        assert_parity(g, run_oracle(est, ro, {}), f"{est} no truncation T={T} "
+                      f"ld=T+{ld_extra} off={offset}")
+
+
 def test_bool_flags():
     ro = sr.generic(8, 333, seed=15, p_term=0.05, p_trunc=0.05)
     for est in ESTIMATORS:
