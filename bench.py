@@ -82,10 +82,24 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM bytes (read + write) per launch measured by ncu, keyed by (hash of the kernel
-# sources at the time of the capture, estimator, N, T, workspace); null once the kernels
-# change. Filled from the ncu summaries under profiles/.
-NCU_TRAFFIC: dict = {}
+# DRAM bytes (read + write) per launch measured by ncu (one captured launch, --set full),
+# keyed by (hash of the kernel sources at the time of the capture, estimator, N, T,
+# workspace); null once the kernels change. Within one captured launch the outputs stay
+# in L2, so these are mostly reads. Summaries with the commands: profiles/*_kernel.md.
+_H = "1afb3712add046c2"
+NCU_TRAFFIC = {
+    (_H, "gae", 4096, 1024, False): 43_940_096,
+    (_H, "return", 4096, 1024, False): 20_995_840,
+    (_H, "td_lambda", 4096, 1024, False): 37_784_320,
+    (_H, "vtrace", 4096, 1024, False): 56_749_056,
+    (_H, "retrace", 4096, 1024, False): 73_251_584,
+    (_H, "td_multi", 4096, 1024, False): 40_129_024,
+    (_H, "trace", 4096, 1024, False): 25_190_912,
+    (_H, "gae_bf16", 4096, 1024, False): 26_243_840,
+    (_H, "retrace", 2048, 4096, False): 154_691_072,
+    (_H, "return", 4096, 128, False): 2_650_880,
+    (_H, "return", 16, 524288, True): 42_610_944,
+}
 
 
 def kernel_source_hash() -> str:
@@ -357,40 +371,107 @@ def per_estimator_roofline(torch, rlca, device, peak):
     return out
 
 
-def e2e_run(torch, rlca, ro, device, n_steps):
-    """Public API end to end: pinned host -> device copies of the step's inputs, the
-    fused GAE call, device -> pinned host copies of advantages and returns."""
+def e2e_run(torch, rlca, ro, device, n_steps, in_streams=1):
+    """Public API end to end: every step copies its inputs from pinned host memory to the
+    device, makes the fused GAE call, and copies advantages and returns back to pinned
+    host memory. Two buffer sets and three streams let step i+1's inputs copy in while
+    step i's results copy out (the link is full duplex); the same steps run once more
+    one after another on one stream for comparison. More input streams were measured
+    and do not help: the host-to-device copies run at about 173 GB/s however they are
+    split."""
     names = ("reward", "value", "terminated", "truncated", "trunc_value", "bootstrap")
-    host = {k: torch.from_numpy(getattr(ro, k)).pin_memory() for k in names}
-    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    adv_h = torch.empty((ro.N, ro.T), dtype=torch.float32).pin_memory()
-    ret_h = torch.empty_like(adv_h).pin_memory()
+    host = [{k: torch.from_numpy(getattr(ro, k)).pin_memory() for k in names}
+            for _ in range(2)]
+    dev = [{k: torch.empty_like(v, device=device) for k, v in host[0].items()}
+           for _ in range(2)]
+    outs = [(torch.empty((ro.N, ro.T), dtype=torch.float32, device=device),
+             torch.empty((ro.N, ro.T), dtype=torch.float32, device=device)) for _ in range(2)]
+    res_h = [(torch.empty((ro.N, ro.T), dtype=torch.float32).pin_memory(),
+              torch.empty((ro.N, ro.T), dtype=torch.float32).pin_memory()) for _ in range(2)]
     params = ro.params
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = 2 * adv_h.numel() * 4
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = 2 * res_h[0][0].numel() * 4
+    s_ins = [torch.cuda.Stream(device) for _ in range(in_streams)]
+    s_run, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    # Input copies spread over the input streams, largest first, to balance their bytes.
+    lanes = [[] for _ in s_ins]
+    load = [0] * len(s_ins)
+    for k in sorted(names, key=lambda k: -host[0][k].numel() * host[0][k].element_size()):
+        j = load.index(min(load))
+        lanes[j].append(k)
+        load[j] += host[0][k].numel() * host[0][k].element_size()
+    ev = lambda: torch.cuda.Event()
+    run_done, out_done = ([ev(), ev()] for _ in range(2))
+    in_ready = [[ev(), ev()] for _ in s_ins]
 
-    def step():
-        for k in names:
-            dev[k].copy_(host[k], non_blocking=True)
-        adv, ret = rlca.rlca_gae(dev["reward"], dev["value"], dev["terminated"],
-                                 dev["truncated"], dev["trunc_value"], dev["bootstrap"],
-                                 gamma=params["gamma"], lam=params["lam"])
-        adv_h.copy_(adv, non_blocking=True)
-        ret_h.copy_(ret, non_blocking=True)
+    def call(b):
+        d = dev[b]
+        rlca.rlca_gae(d["reward"], d["value"], d["terminated"], d["truncated"],
+                      d["trunc_value"], d["bootstrap"], gamma=params["gamma"],
+                      lam=params["lam"], advantages=outs[b][0], returns=outs[b][1])
 
-    for _ in range(2):
-        step()
+    def step(i):
+        b = i & 1
+        for j, st in enumerate(s_ins):
+            with torch.cuda.stream(st):
+                st.wait_event(run_done[b])  # the call two steps back has read these inputs
+                for k in lanes[j]:
+                    dev[b][k].copy_(host[b][k], non_blocking=True)
+                in_ready[j][b].record(st)
+        with torch.cuda.stream(s_run):
+            for j in range(len(s_ins)):
+                s_run.wait_event(in_ready[j][b])
+            s_run.wait_event(out_done[b])  # results two steps back have been copied out
+            call(b)
+            run_done[b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(run_done[b])
+            res_h[b][0].copy_(outs[b][0], non_blocking=True)
+            res_h[b][1].copy_(outs[b][1], non_blocking=True)
+            out_done[b].record(s_out)
+
+    def timed(run_steps):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(device)
+        e0.record(cur)
+        for st in (*s_ins, s_run, s_out):
+            st.wait_event(e0)
+        run_steps()
+        for st in (*s_ins, s_run, s_out):
+            cur.wait_stream(st)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    for i in range(4):
+        step(i)
+    ms = timed(lambda: [step(i) for i in range(n_steps)])
+
+    def serial():
+        with torch.cuda.stream(s_run):
+            for _ in range(n_steps):
+                for k in names:
+                    dev[0][k].copy_(host[0][k], non_blocking=True)
+                call(0)
+                res_h[0][0].copy_(outs[0][0], non_blocking=True)
+                res_h[0][1].copy_(outs[0][1], non_blocking=True)
+    ms_serial = timed(serial)
+    # The last step's results match a plain call on the same inputs.
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n_steps):
-        step()
-    e1.record()
+    b = (n_steps - 1) & 1
+    call(b)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ok = bool(torch.equal(res_h[b][0], outs[b][0].cpu()) and
+              torch.equal(res_h[b][1], outs[b][1].cpu()))
     return {"value": round(ro.N * ro.T * n_steps / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
-            "ms_per_step": round(ms / n_steps, 4)}
+            "ms_per_step": round(ms / n_steps, 4),
+            "mode": "double-buffered: step i+1's inputs copy in while step i runs and its "
+                    "results copy out (3 streams, pinned host buffers)",
+            "serial_value": round(ro.N * ro.T * n_steps / (ms_serial * 1e-3), 1),
+            "serial_ms_per_step": round(ms_serial / n_steps, 4),
+            "results_checked": ok}
 
 
 def cpu_baseline(ro, seconds):
@@ -574,7 +655,7 @@ def main():
     ap.add_argument("--seq-len", type=int, default=SEQ_LEN)
     ap.add_argument("--estimator", choices=tuple(WORKLOADS), default="gae",
                     help="estimator timed in the main loop (the metric's workload is gae)")
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--workspace", action="store_true",
