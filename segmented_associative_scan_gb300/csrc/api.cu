@@ -98,14 +98,22 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
 
     // 128-bit loads/stores need 16-byte aligned rows: ld a multiple of 16 bytes of every
     // array (ld % 4 == 0 for fp32, ld % 8 == 0 for bf16 inputs) and aligned bases.
-    bool vec = (p.ld % (int64_t)(16 / in_elem)) == 0 && aligned(p.term, 4) &&
-               (!p.trunc || aligned(p.trunc, 4));
-    for (int i = 0; i < n_in; ++i) vec = vec && aligned(f32_in[i], 16);
-    for (int o = 0; o < n_out; ++o) vec = vec && (!outs[o] || aligned(outs[o], 16));
+    bool vec16 = (p.ld % (int64_t)(16 / in_elem)) == 0 && aligned(p.term, 4) &&
+                 (!p.trunc || aligned(p.trunc, 4));
+    for (int i = 0; i < n_in; ++i) vec16 = vec16 && aligned(f32_in[i], 16);
+    for (int o = 0; o < n_out; ++o) vec16 = vec16 && (!outs[o] || aligned(outs[o], 16));
+    // 256-bit access to fp32 rows (8 steps per thread in one access) needs 32-byte
+    // aligned rows: ld % 8 == 0, fp32 bases 32-byte aligned, flag bases 8-byte aligned
+    // (bf16 inputs keep 128-bit loads; only the fp32 outputs widen then).
+    bool vec32 = vec16 && (p.ld % 8) == 0 && aligned(p.term, 8) &&
+                 (!p.trunc || aligned(p.trunc, 8));
+    for (int i = 0; i < n_in; ++i) vec32 = vec32 && (in_elem == 2 || aligned(f32_in[i], 32));
+    for (int o = 0; o < n_out; ++o) vec32 = vec32 && (!outs[o] || aligned(outs[o], 32));
+    const int vec = vec32 ? 2 : (vec16 ? 1 : 0);
 
     // The warp-streaming kernel moves chunks with 16-byte bulk copies: every base
     // 16-byte aligned, ld and T multiples of 16, and packed rows contiguous (ld == T).
-    bool streamable = in_elem == 4 && vec && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
+    bool streamable = in_elem == 4 && vec16 && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
                       (p.T > rlca::kWarpChunk || p.ld == p.T) && aligned(p.term, 16) &&
                       (!p.trunc || aligned(p.trunc, 16));
 
@@ -140,7 +148,7 @@ Params base_params(const float *reward, const uint8_t *term, const uint8_t *trun
 template <typename F>
 auto bf16_launch(F fn)
 {
-    return [fn](const Params &q, bool vec, bool, cudaStream_t s) { return fn(q, vec, s); };
+    return [fn](const Params &q, int vec, bool, cudaStream_t s) { return fn(q, vec, s); };
 }
 
 int discounted_return(const float *reward, const uint8_t *terminated, const uint8_t *truncated,
@@ -273,7 +281,7 @@ int td_lambda_multi(const float *reward, const float *value, const uint8_t *term
         for (int k = 0; k < n_lambdas; ++k)
             if (!outs[k]) return RLCA_ERR_NULL;
     const float *in[] = {reward, value};
-    auto launch = [](const Params &q, bool vec, bool, cudaStream_t s) {
+    auto launch = [](const Params &q, int vec, bool, cudaStream_t s) {
         return rlca::launch_td_multi(q, vec, s);
     };
     return validate_and_launch(p, in, 2, outs, n_lambdas, Workspace{nullptr, 0}, launch,
@@ -293,7 +301,7 @@ int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *trunc
     p.out0 = out;
     const float *in[] = {x};
     float *outs[] = {out};
-    auto launch = [bf16](const Params &q, bool vec, bool, cudaStream_t s) {
+    auto launch = [bf16](const Params &q, int vec, bool, cudaStream_t s) {
         return bf16 ? rlca::launch_forward_bf16(q, vec, s) : rlca::launch_forward(q, vec, s);
     };
     return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream,

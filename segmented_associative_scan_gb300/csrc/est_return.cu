@@ -3,12 +3,12 @@
 #include "launch.cuh"
 
 namespace rlca {
-cudaError_t launch_return(const Params &p, bool vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_return(const Params &p, int vec, bool streamable, cudaStream_t stream)
 {
     return launch_estimator<Est::kReturn>(p, vec, streamable, stream);
 }
 
-cudaError_t launch_return_bf16(const Params &p, bool vec, cudaStream_t stream)
+cudaError_t launch_return_bf16(const Params &p, int vec, cudaStream_t stream)
 {
     return launch_estimator_bf16<Est::kReturn>(p, vec, stream);
 }

@@ -3,17 +3,17 @@
 #include "launch.cuh"
 
 namespace rlca {
-cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_td_lambda(const Params &p, int vec, bool streamable, cudaStream_t stream)
 {
     return launch_estimator<Est::kTdLambda>(p, vec, streamable, stream);
 }
 
-cudaError_t launch_td_lambda_bf16(const Params &p, bool vec, cudaStream_t stream)
+cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream)
 {
     return launch_estimator_bf16<Est::kTdLambda>(p, vec, stream);
 }
 // Fused TD(lambda) for several lambdas: whole-row CTA tiles, or the row loop.
-template <bool VEC, bool TRUNC>
+template <int VEC, bool TRUNC>
 cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
 {
     if (p.T <= kTile) {
@@ -35,7 +35,7 @@ cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
                       (unsigned)p.N, kThreads, 0, stream, p);
 }
 
-cudaError_t launch_td_multi(const Params &p_in, bool vec, cudaStream_t stream)
+cudaError_t launch_td_multi(const Params &p_in, int vec, cudaStream_t stream)
 {
     Params p = p_in;
     for (int k = 0; k < p.multi.count; ++k) {
@@ -45,11 +45,9 @@ cudaError_t launch_td_multi(const Params &p_in, bool vec, cudaStream_t stream)
         p.multi.beta_pow[k] = pw;
     }
     const bool trunc = p.trunc != nullptr;
-    if (vec)
-        return trunc ? launch_td_multi_variant<true, true>(p, stream)
-                     : launch_td_multi_variant<true, false>(p, stream);
-    return trunc ? launch_td_multi_variant<false, true>(p, stream)
-                 : launch_td_multi_variant<false, false>(p, stream);
+    return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
+        return launch_td_multi_variant<decltype(v)::value, decltype(r)::value>(p, stream);
+    });
 }
 
 }  // namespace rlca

@@ -123,7 +123,7 @@ __device__ __forceinline__ float next_item(float first_item, const TIn *__restri
     return need ? s : 0.f;
 }
 
-template <Est E, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
+template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0, bool active,
                                            int lane, Chunk<ITEMS> &c)
 {
@@ -258,7 +258,7 @@ __device__ __forceinline__ void replay(const Params &p, const Chunk<ITEMS> &c,
 }
 
 // Outputs of every item from A_t (A[j]) and A at the step after the chunk (a_after).
-template <Est E, int ITEMS, bool VEC>
+template <Est E, int ITEMS, int VEC>
 __device__ __forceinline__ void epilogue(const Params &p, const Chunk<ITEMS> &c,
                                          const float (&A)[ITEMS], float a_after, int64_t row,
                                          int t0)

@@ -23,7 +23,7 @@ namespace rlca {
 // One chunk: A at the step before the chunk is `carry_in`; `prev_ended` says whether the
 // step before lane 0's first step ended an episode. Returns A at the chunk's last step;
 // *last_ended gets whether that step ended an episode.
-template <int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
+template <int ITEMS, int VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int t0, bool active,
                                                float carry_in, bool prev_ended,
                                                bool *last_ended)
@@ -83,7 +83,7 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
     return affine_apply(whole, carry_in);
 }
 
-template <int ITEMS, bool VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
+template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
 __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params p)
 {
     grid_dependency_sync();
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
 // belongs to the previous warp, so the warp scans as if it did not, and the flag is
 // applied after the exchange instead: the warp's carry-in becomes 0 (its first step then
 // equals x exactly) and its total is marked as a reset for the warps after it.
-template <int NT, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
+template <int NT, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int t0, bool active,
                                               float carry_in, bool prev_ended, bool *last_ended,
                                               ScanSmem<NT> &sm, int buf)
@@ -197,7 +197,7 @@ __device__ __forceinline__ float forward_tile(const Params &p, int64_t row, int 
 
 // CTA-tiled forward scan: T <= NT * ITEMS packs whole rows into a tile; longer rows are
 // walked tile by tile from the first, with the carry in registers.
-template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, typename TIn = float>
+template <int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL, typename TIn = float>
 __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;

@@ -145,7 +145,7 @@ __device__ __forceinline__ float lookback_carry(const Params &p, int64_t row, in
 // Scan the loaded steps this thread owns, write the outputs and return A at the tile's
 // first step. The tile's carry-in (A at the step after the tile) is `carry_in`, or,
 // with LB, the result of the look-back (`epoch` and `seg` identify the tile's state).
-template <Est E, int NT, int ITEMS, bool VEC, bool LB, typename TIn = float>
+template <Est E, int NT, int ITEMS, int VEC, bool LB, typename TIn = float>
 __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, int64_t row,
                                             int t0, float carry_in, ScanSmem<NT> &sm, int buf,
                                             int seg = 0, unsigned epoch = 0)
@@ -207,7 +207,7 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
 }
 
 // Load this thread's steps from global memory, then scan_chunk.
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, bool LB, typename TIn = float>
+template <Est E, int NT, int ITEMS, int VEC, bool TRUNC, bool LB, typename TIn = float>
 __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
                                            float carry_in, ScanSmem<NT> &sm, int buf,
                                            int seg = 0, unsigned epoch = 0)
@@ -227,7 +227,7 @@ __device__ __forceinline__ void grid_dependency_sync()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <Est E, int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL, int MINB = 1,
+template <Est E, int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL, int MINB = 1,
           typename TIn = float>
 __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
 {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
 // TD(lambda) for p.multi.count lambdas from one load of a tile: the chunk is read once,
 // then built, scanned and stored once per lambda (each scan alternates the shared
 // buffers, so consecutive scans never race on them).
-template <int NT, int ITEMS, bool VEC, bool TRUNC, Tiling TL>
+template <int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL>
 __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
 // aggregates, a warp suffix scan, and the chunk's carry-in (A at the step after the
 // chunk) applied directly. Returns A at the chunk's first step.
-template <Est E, int ITEMS, bool VEC, bool TRUNC, typename TIn = float>
+template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
 __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0, bool active,
                                             float carry_in)
 {
@@ -358,7 +358,7 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
 //   first with the carry in a register.
 // All warps of a typical launch are resident at once, so each keeps its next chunk's
 // loads in flight without any cross-warp wait.
-template <Est E, int ITEMS, bool VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
+template <Est E, int ITEMS, int VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
 __global__ void __launch_bounds__(32 * WARPS) credit_warp_kernel(const Params p)
 {
     grid_dependency_sync();

@@ -100,7 +100,7 @@ inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool t
 
 // ------------------------------------------------------------------ CTA tile paths
 
-template <Est E, bool VEC, bool TRUNC, typename TIn = float>
+template <Est E, int VEC, bool TRUNC, typename TIn = float>
 cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 {
     if (path == Path::kCtaRows) {
@@ -131,7 +131,7 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 
 // ------------------------------------------------------------------ warp paths
 
-template <Est E, bool VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
+template <Est E, int VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
 cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * ITEMS;
@@ -201,7 +201,39 @@ cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
 
 // ------------------------------------------------------------------ dispatch
 
-template <Est E, bool VEC, bool TRUNC>
+// Access widths. Rows that allow 256-bit access (32-byte aligned, access level 2) use
+// 256-bit loads and stores (kWideVec) unless measured slower. Measured on GB300, 128-bit
+// vs 256-bit loads and stores, in us per launch:
+//   warp-owned rows [4096, 128]: return 2.23 vs 2.14, TD(lambda) 2.36 vs 2.26, V-trace
+//     3.86 vs 3.48, Retrace 3.37 vs 2.52, GAE 2.97 vs 2.51, fused TD 4.21 vs 3.93;
+//   row loop [2048, 4096]: return 15.79 vs 15.43, TD 19.90 vs 19.10, V-trace 32.46 vs
+//     31.38, Retrace 30.77 vs 27.63, GAE 24.86 vs 23.51, fused TD 33.82 vs 32.45;
+//   one row per CTA [4096, 1024]: return 7.71 vs 7.52, GAE 12.52 vs 12.05, V-trace 16.88
+//     vs 16.70, fused TD 17.33 vs 17.11, but TD 10.07 vs 10.16, Retrace 15.22 vs 15.36
+//     and the forward scan 8.46 vs 8.53, which keep 128-bit access there;
+//   the warp-streaming GAE (stores only) 14.48 vs 15.16: it keeps 128-bit stores.
+// Wide loads alone or wide stores alone were slower than either.
+constexpr int kWideVec = kVec16 | kWideLoads | kWideStores;
+
+// Calls f(integral_constant<int, V>, integral_constant<bool, R>) with the access width for
+// the run-time level `vec` (0 scalar, 1 128-bit, 2 kWideVec) and the truncation flag.
+template <class F>
+cudaError_t with_vec_trunc(int vec, bool trunc, F &&f)
+{
+    using V0 = std::integral_constant<int, 0>;
+    using V1 = std::integral_constant<int, kVec16>;
+    using V2 = std::integral_constant<int, kWideVec>;
+    using R1 = std::true_type;
+    using R0 = std::false_type;
+    if (vec >= 2) return trunc ? f(V2{}, R1{}) : f(V2{}, R0{});
+    if (vec == 1) return trunc ? f(V1{}, R1{}) : f(V1{}, R0{});
+    return trunc ? f(V0{}, R1{}) : f(V0{}, R0{});
+}
+
+// True when a CTA tile holds exactly one row (TILE / 2 < T <= TILE).
+inline bool one_row_per_cta(int T) { return 2 * T > kTile && T <= kTile; }
+
+template <Est E, int VEC, bool TRUNC>
 cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
 {
     if (path == Path::kWarpRows) return launch_warp_rows<E, VEC, TRUNC>(p, stream);
@@ -222,40 +254,38 @@ void set_beta_pow(Params &p)
 // one warp chunk, CTA tiles (whole rows or the row loop) beyond; GAE rows longer than a
 // warp chunk go to warp-owned rows with 16 steps per lane (measured fastest for bf16).
 template <Est E>
-cudaError_t launch_estimator_bf16(const Params &p_in, bool vec, cudaStream_t stream)
+cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stream)
 {
     Params p = p_in;
     set_beta_pow<E>(p);
+    const bool trunc = p.trunc != nullptr;
+    // bf16 data loads stay 128-bit; wide flag loads and output stores were measured
+    // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout.
+    vec = vec < 1 ? vec : 1;
     if (E == Est::kGae && p.T > 32 * kItems) {
         // 16 steps per lane: beta^16 for the per-lane composite.
         p.beta_pow = p.gamma_lambda;
         for (int i = 1; i < 16; ++i) p.beta_pow = p.gamma_lambda * p.beta_pow;
-        const bool trunc = p.trunc != nullptr;
-        if (vec)
-            return trunc ? launch_warp_rows<E, true, true, uint16_t, 16>(p, stream)
-                         : launch_warp_rows<E, true, false, uint16_t, 16>(p, stream);
-        return trunc ? launch_warp_rows<E, false, true, uint16_t, 16>(p, stream)
-                     : launch_warp_rows<E, false, false, uint16_t, 16>(p, stream);
+        return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
+            return launch_warp_rows<E, decltype(v)::value, decltype(r)::value, uint16_t, 16>(
+                p, stream);
+        });
     }
-    const bool trunc = p.trunc != nullptr;
     const Path path = p.T <= 32 * kItems ? Path::kWarpRows
                                          : (p.T > kTile ? Path::kCtaRowLoop : Path::kCtaRows);
-    auto go = [&](auto vec_tag, auto trunc_tag) {
-        constexpr bool V = decltype(vec_tag)::value;
-        constexpr bool R = decltype(trunc_tag)::value;
+    return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
+        constexpr int V = decltype(v)::value;
+        constexpr bool R = decltype(r)::value;
         if (path == Path::kWarpRows) return launch_warp_rows<E, V, R, uint16_t>(p, stream);
         return launch_cta<E, V, R, uint16_t>(p, path, stream);
-    };
-    using T_ = std::true_type;
-    using F_ = std::false_type;
-    if (vec) return trunc ? go(T_{}, T_{}) : go(T_{}, F_{});
-    return trunc ? go(F_{}, T_{}) : go(F_{}, F_{});
+    });
 }
 
-// Launch one estimator; `vec` = 16-byte aligned rows (128-bit access), `streamable` =
-// layout fit for 16-byte bulk copies (see api.cu).
+// Launch one estimator; `vec` = access level (0 scalar, 1 16-byte aligned rows with
+// 128-bit access, 2 32-byte aligned rows fit for 256-bit access), `streamable` = layout
+// fit for 16-byte bulk copies (see api.cu).
 template <Est E>
-cudaError_t launch_estimator(const Params &p_in, bool vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_estimator(const Params &p_in, int vec, bool streamable, cudaStream_t stream)
 {
     Params p = p_in;
     set_beta_pow<E>(p);
@@ -264,29 +294,30 @@ cudaError_t launch_estimator(const Params &p_in, bool vec, bool streamable, cuda
     if (path == Path::kWarpStream)
         return trunc ? launch_warp_stream<E, true>(p, stream)
                      : launch_warp_stream<E, false>(p, stream);
-    if (vec)
-        return trunc ? launch_path<E, true, true>(p, path, stream)
-                     : launch_path<E, true, false>(p, path, stream);
-    return trunc ? launch_path<E, false, true>(p, path, stream)
-                 : launch_path<E, false, false>(p, path, stream);
+    if ((E == Est::kTdLambda || E == Est::kRetrace) && path == Path::kCtaRows &&
+        one_row_per_cta(p.T))
+        vec = vec < 1 ? vec : 1;
+    return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
+        return launch_path<E, decltype(v)::value, decltype(r)::value>(p, path, stream);
+    });
 }
 
 // One definition per estimator, each in its own translation unit.
-cudaError_t launch_return(const Params &p, bool vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_td_lambda(const Params &p, bool vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_gae(const Params &p, bool vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_vtrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_retrace(const Params &p, bool vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_return(const Params &p, int vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_td_lambda(const Params &p, int vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_gae(const Params &p, int vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_vtrace(const Params &p, int vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_retrace(const Params &p, int vec, bool streamable, cudaStream_t stream);
 // The same with bf16 per-step inputs.
-cudaError_t launch_return_bf16(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_td_lambda_bf16(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_gae_bf16(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_vtrace_bf16(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_retrace_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_return_bf16(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_gae_bf16(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_vtrace_bf16(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_retrace_bf16(const Params &p, int vec, cudaStream_t stream);
 // Fused TD(lambda) for p.multi.count lambdas (outputs in p.multi.out).
-cudaError_t launch_td_multi(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_td_multi(const Params &p, int vec, cudaStream_t stream);
 // Forward scans: p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
-cudaError_t launch_forward(const Params &p, bool vec, cudaStream_t stream);
-cudaError_t launch_forward_bf16(const Params &p, bool vec, cudaStream_t stream);
+cudaError_t launch_forward(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_forward_bf16(const Params &p, int vec, cudaStream_t stream);
 
 }  // namespace rlca

@@ -74,6 +74,34 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t *p) { return __ldcs
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(float *p, float v) { __stcs(p, v); }
 
+// Access widths, the VEC template argument of the load/store helpers (bit flags):
+//   0 scalar; bit 0: 128-bit access (16-byte aligned rows);
+//   bit 1: 256-bit loads of fp32 data and 64-bit loads of the 8 flag bytes of 8 steps;
+//   bit 2: 256-bit stores of fp32 outputs.
+// Bits 1 and 2 need 32-byte aligned rows (sm_100 and later). A 256-bit access moves one
+// whole 32-byte sector per thread, so a warp's store fills every sector it touches in
+// one instruction instead of writing two half sectors.
+constexpr int kVec16 = 1;
+constexpr int kWideLoads = 2;
+constexpr int kWideStores = 4;
+__device__ __forceinline__ void ld_stream8(const float *p, float *x)
+{
+    asm volatile("ld.global.cs.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]),
+                   "=f"(x[6]), "=f"(x[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_stream8(float *p, const float *x)
+{
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                 "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                 "f"(x[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_stream(const uint2 *p) { return __ldcs(p); }
+
 template <int ITEMS>
 __device__ __forceinline__ constexpr unsigned all_items()
 {
@@ -138,14 +166,20 @@ struct InType<uint16_t> {
 };
 
 // ITEMS consecutive inputs of one row starting at column t0, widened to fp32; columns
-// >= T read as 0. VEC: 128-bit loads (the row start and t0 are 16-byte aligned).
-template <int ITEMS, bool VEC, typename TIn = float>
+// >= T read as 0. VEC 1: 128-bit loads (the row start and t0 are 16-byte aligned);
+// VEC bit 1: 256-bit loads for fp32 data (32-byte aligned), 128-bit for bf16.
+template <int ITEMS, int VEC, typename TIn = float>
 __device__ __forceinline__ void load_items(const TIn *__restrict__ row, int t0, int T,
                                            float (&x)[ITEMS])
 {
     constexpr int PV = InType<TIn>::kPerVec;
     static_assert(ITEMS % PV == 0, "a thread's items fill whole 128-bit loads");
-    if (VEC && t0 + ITEMS <= T) {
+    constexpr bool kWide = (VEC & kWideLoads) && sizeof(TIn) == 4 && ITEMS % 8 == 0;
+    if (kWide && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 8; ++k)
+            ld_stream8(reinterpret_cast<const float *>(row + t0) + 8 * k, x + 8 * k);
+    } else if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
         for (int k = 0; k < ITEMS / PV; ++k) {
             const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(row + t0) + k);
@@ -168,13 +202,20 @@ __device__ __forceinline__ unsigned nonzero_bytes(uint32_t w)
     return (b * 0x01020408u) >> 24;
 }
 
-// Bit j set when flag byte (t0 + j) is nonzero; columns >= T read as clear.
-template <int ITEMS, bool VEC>
+// Bit j set when flag byte (t0 + j) is nonzero; columns >= T read as clear. VEC bit 1
+// reads the 8 bytes of 8 steps with one 64-bit load (row start and t0 8-byte aligned).
+template <int ITEMS, int VEC>
 __device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ row, int t0,
                                                    int T)
 {
     unsigned bits = 0;
-    if (VEC && t0 + ITEMS <= T) {
+    if ((VEC & kWideLoads) && ITEMS % 8 == 0 && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 8; ++k) {
+            const uint2 w = ld_stream(reinterpret_cast<const uint2 *>(row + t0) + k);
+            bits |= (nonzero_bytes(w.x) | (nonzero_bytes(w.y) << 4)) << (8 * k);
+        }
+    } else if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k)
             bits |= nonzero_bytes(ld_stream(reinterpret_cast<const uint32_t *>(row + t0) + k))
@@ -189,13 +230,20 @@ __device__ __forceinline__ unsigned load_flag_bits(const uint8_t *__restrict__ r
 
 // Bit j set when either flag byte (t0 + j) of row_a or row_b is nonzero: the two flag
 // words are OR-ed before a single decode.
-template <int ITEMS, bool VEC>
+template <int ITEMS, int VEC>
 __device__ __forceinline__ unsigned load_flag_bits_or(const uint8_t *__restrict__ row_a,
                                                       const uint8_t *__restrict__ row_b, int t0,
                                                       int T)
 {
     unsigned bits = 0;
-    if (VEC && t0 + ITEMS <= T) {
+    if ((VEC & kWideLoads) && ITEMS % 8 == 0 && t0 + ITEMS <= T) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 8; ++k) {
+            const uint2 a = ld_stream(reinterpret_cast<const uint2 *>(row_a + t0) + k);
+            const uint2 b = ld_stream(reinterpret_cast<const uint2 *>(row_b + t0) + k);
+            bits |= (nonzero_bytes(a.x | b.x) | (nonzero_bytes(a.y | b.y) << 4)) << (8 * k);
+        }
+    } else if (VEC && t0 + ITEMS <= T) {
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k)
             bits |= nonzero_bytes(ld_stream(reinterpret_cast<const uint32_t *>(row_a + t0) + k) |
@@ -210,11 +258,14 @@ __device__ __forceinline__ unsigned load_flag_bits_or(const uint8_t *__restrict_
 }
 
 // Store the valid items (bit j of `valid`) of ITEMS consecutive floats.
-template <int ITEMS, bool VEC>
+template <int ITEMS, int VEC>
 __device__ __forceinline__ void store_items(float *__restrict__ row, int t0, unsigned valid,
                                             const float (&x)[ITEMS])
 {
-    if (VEC && valid == all_items<ITEMS>()) {
+    if ((VEC & kWideStores) && ITEMS % 8 == 0 && valid == all_items<ITEMS>()) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 8; ++k) st_stream8(row + t0 + 8 * k, x + 8 * k);
+    } else if (VEC && valid == all_items<ITEMS>()) {
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k)
             st_stream(reinterpret_cast<float4 *>(row + t0) + k,

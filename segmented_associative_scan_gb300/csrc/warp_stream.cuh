@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_stream_kernel(const Pa
         const float a_after = affine_apply(excl, carry_in);
         float A[ITEMS];
         replay<E, ITEMS>(p, c, e, a_after, A);
-        epilogue<E, ITEMS, true>(p, c, A, a_after, row, t0);
+        epilogue<E, ITEMS, kVec16>(p, c, A, a_after, row, t0);
         carry = affine_apply(whole, carry_in);
         warp_advance(p, cons);
     }

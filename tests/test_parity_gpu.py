@@ -172,6 +172,18 @@ def test_without_truncation(ld_extra, offset, T):
                       f"ld=T+{ld_extra} off={offset}")
 
 
+@pytest.mark.parametrize("ld_extra,offset", [(0, 0), (16, 0), (16, 4), (8, 2), (4, 0)])
+@pytest.mark.parametrize("T", [256, 1024, 2048])
+def test_access_widths(ld_extra, offset, T):
+    """Each access width on the same inputs: 256-bit (32-byte aligned rows: ld % 8 == 0,
+    offset 0), 128-bit (offset 4 floats or ld % 8 == 4), scalar (offset 2). For GAE with
+    truncation at T = 1024 the warp-streaming kernel takes both store widths."""
+    ro = sr.generic(29, T, seed=70 + T + ld_extra + offset, p_term=0.01, p_trunc=0.005)
+    for est in ESTIMATORS:
+        g = run_gpu(est, ro, {}, ld=T + ld_extra, offset=offset)
+        assert_parity(g, run_oracle(est, ro, {}), f"{est} T={T} ld=T+{ld_extra} off={offset}")
+
+
 def test_bool_flags():
     ro = sr.generic(8, 333, seed=15, p_term=0.05, p_trunc=0.05)
     for est in ESTIMATORS:
