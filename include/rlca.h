@@ -16,7 +16,7 @@
  *     bootstraps from a supplied per-env value, counted exactly once.
  *
  * Common conventions (all entry points)
- *   Layout    Every per-step array is row-major [N, ld] in device memory: row n holds
+ *   Layout    Every per-step array is row-major [N, ld]: row n holds
  *             env n, steps t = 0..T-1 in columns 0..T-1 (T contiguous), ld >= T.
  *             Outputs use the same layout and ld; their columns T..ld-1 are not
  *             written. Data are float32; flags are uint8 (0 = clear, nonzero = set;
@@ -27,9 +27,18 @@
  *             where truncated is set. If both are set, termination wins. At t = T-1 the
  *             successor value is bootstrap[n] (nullable = 0) unless the step is
  *             terminated or truncated.
+ *   Memory    Every buffer is either device memory of the current device (cudaMalloc,
+ *             a stream-ordered pool, managed memory) or pinned host memory
+ *             (cudaHostAlloc, cudaMallocHost, cudaHostRegister; torch pin_memory). On
+ *             GB300 the kernels read and write pinned host memory directly over
+ *             NVLink-C2C, so a caller whose rollouts sit in host memory needs no
+ *             staging copies: inputs cross the link once and outputs once, inside the
+ *             kernel. Pageable host memory and another device's memory are rejected
+ *             with RLCA_ERR_MEMORY (each pointer is classified with
+ *             cudaPointerGetAttributes on every call). The look-back workspace must be
+ *             device memory.
  *   Stream    `stream` is a cudaStream_t (NULL = the legacy default stream) of the
- *             current device; all work is enqueued on it, asynchronously. Pointers must
- *             belong to the current device.
+ *             current device; all work is enqueued on it, asynchronously.
  *   Ownership The caller owns every buffer. The library never allocates or frees
  *             memory, never changes the current device and never synchronises (except
  *             rlca_workspace_check, which says so). Inputs are read only. Outputs must
@@ -59,7 +68,8 @@ enum rlca_status {
     RLCA_ERR_ALIAS = -4,     /* an output overlaps an input or another output */
     RLCA_ERR_WORKSPACE = -5, /* workspace too small or misaligned */
     RLCA_ERR_LAUNCH = -6,    /* the CUDA launch failed */
-    RLCA_ERR_TIMEOUT = -7    /* a bounded cross-block wait gave up (see rlca_workspace_check) */
+    RLCA_ERR_TIMEOUT = -7,   /* a bounded cross-block wait gave up (see rlca_workspace_check) */
+    RLCA_ERR_MEMORY = -8     /* a buffer is neither current-device memory nor pinned host memory */
 };
 
 /* Largest supported seq_len. */

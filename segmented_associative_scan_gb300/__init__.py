@@ -7,11 +7,14 @@ fallback: if the library is not built, every call raises.
 
 The functions carry the names of the C entry points (``include/rlca.h``) and take
 torch tensors:
-  - per-step tensors: CUDA, 2-D [N, T], unit stride along T, all with the same row
-    stride; float32 data (or all bfloat16, which selects the _bf16 entry points), uint8
-    or bool flags;
-  - per-env bootstrap values: CUDA float32 [N] (optional);
-  - outputs are allocated (same row stride as the inputs) unless passed in.
+  - per-step tensors: 2-D [N, T], unit stride along T, all with the same row stride;
+    float32 data (or all bfloat16, which selects the _bf16 entry points), uint8 or
+    bool flags;
+  - per-env bootstrap values: float32 [N] (optional);
+  - every tensor is on one CUDA device or in pinned host memory (read and written in
+    place by the kernels over NVLink-C2C);
+  - outputs are allocated (same row stride as the inputs; pinned host memory when the
+    reward tensor is there) unless passed in.
 Work is enqueued on ``torch.cuda.current_stream()``; nothing synchronises.
 """
 from __future__ import annotations
@@ -97,22 +100,37 @@ def _check(fn: str, status: int):
 
 
 class _Rows:
-    """Shape/stride bookkeeping shared by the per-step tensors of one call."""
+    """Shape/stride bookkeeping shared by the per-step tensors of one call.
+
+    Tensors live on one CUDA device, or in pinned host memory, which the kernels read
+    and write in place (mixing the two is allowed). A call whose first per-step tensor
+    is in pinned host memory runs on the current CUDA device and allocates missing
+    outputs in pinned host memory."""
 
     def __init__(self, ref: torch.Tensor):
         if ref.dim() != 2:
             raise ValueError("per-step tensors must be 2-D [num_envs, seq_len]")
         self.N, self.T = ref.shape
         self.ld = ref.stride(0) if self.N > 1 else max(ref.stride(0), self.T)
-        self.device = ref.device
+        self.host = not ref.is_cuda
+        if self.host and not ref.is_pinned():
+            raise ValueError("host tensors must be in pinned memory (pin_memory())")
+        self.device = (torch.device("cuda", torch.cuda.current_device()) if self.host
+                       else ref.device)
+
+    def _reachable(self, t, name):
+        if t.is_cuda:
+            if t.device != self.device:
+                raise ValueError(f"{name} must be on {self.device} or in pinned host memory")
+        elif not t.is_pinned():
+            raise ValueError(f"{name} must be on {self.device} or in pinned host memory")
 
     def ptr(self, t, name, dtypes, optional=False):
         if t is None:
             if optional:
                 return None
             raise ValueError(f"{name} is required")
-        if not t.is_cuda or t.device != self.device:
-            raise ValueError(f"{name} must be on {self.device}")
+        self._reachable(t, name)
         if t.dtype not in dtypes:
             raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
         if tuple(t.shape) != (self.N, self.T):
@@ -126,16 +144,18 @@ class _Rows:
     def vec_ptr(self, t, name):
         if t is None:
             return None
-        if not t.is_cuda or t.dtype != torch.float32 or t.dim() != 1 or t.shape[0] != self.N:
-            raise ValueError(f"{name} must be a CUDA float32 [{self.N}] tensor")
+        self._reachable(t, name)
+        if t.dtype != torch.float32 or t.dim() != 1 or t.shape[0] != self.N:
+            raise ValueError(f"{name} must be a float32 [{self.N}] tensor")
         if self.N > 1 and t.stride(0) != 1:
             raise ValueError(f"{name} must be contiguous")
         return t.data_ptr() or None
 
     def out(self, t, name):
         if t is None:
-            buf = torch.empty((self.N, max(self.ld, self.T)), dtype=torch.float32,
-                              device=self.device)
+            shape = (self.N, max(self.ld, self.T))
+            buf = (torch.empty(shape, dtype=torch.float32, pin_memory=True) if self.host
+                   else torch.empty(shape, dtype=torch.float32, device=self.device))
             t = buf[:, :self.T]
         self.ptr(t, name, (torch.float32,))
         return t

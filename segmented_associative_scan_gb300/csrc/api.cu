@@ -46,6 +46,31 @@ struct Workspace {
     size_t bytes;
 };
 
+// Where a buffer lives, as the kernels see it.
+enum class Mem { kDevice, kHost, kBad };
+
+// Device memory of the current device (including managed memory) or pinned host memory
+// mapped into the device's address space at the same address (unified addressing).
+// Pageable host memory and other devices' memory are kBad.
+Mem classify(const void *ptr, int device)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Mem::kBad;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        return a.device == device ? Mem::kDevice : Mem::kBad;
+    case cudaMemoryTypeManaged:
+        return Mem::kDevice;
+    case cudaMemoryTypeHost:
+        return a.devicePointer == ptr ? Mem::kHost : Mem::kBad;
+    default:
+        return Mem::kBad;
+    }
+}
+
 // Common validation of inputs, outputs and workspace, then launch.
 // `f32_in` are the required float inputs, `outs` the outputs (outs[0] required).
 // `in_elem`: bytes per element of the per-step data inputs (4 = fp32, 2 = bf16).
@@ -96,6 +121,34 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
         if (p.spin_limit <= 0) p.spin_limit = rlca::kDefaultSpinLimit;
     }
 
+    // Checked last, as it asks the driver: every buffer must be reachable from the
+    // current device. Pinned host memory is read and written in place (no bulk copies
+    // from it: the kernels then use plain loads and stores).
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RLCA_ERR_LAUNCH;
+    }
+    {
+        const void *bufs[12];
+        int nb = 0;
+        for (int i = 0; i < n_in; ++i) bufs[nb++] = f32_in[i];
+        bufs[nb++] = p.term;
+        if (p.trunc) bufs[nb++] = p.trunc;
+        if (p.trunc_value) bufs[nb++] = p.trunc_value;
+        if (p.boot) bufs[nb++] = p.boot;
+        for (int o = 0; o < n_out; ++o)
+            if (outs[o]) bufs[nb++] = outs[o];
+        p.host = 0;
+        for (int i = 0; i < nb; ++i) {
+            const Mem m = classify(bufs[i], device);
+            if (m == Mem::kBad) return RLCA_ERR_MEMORY;
+            if (m == Mem::kHost) p.host = 1;
+        }
+        // The look-back state lives in device memory (its waits poll it).
+        if (p.ws && classify(p.ws, device) != Mem::kDevice) return RLCA_ERR_MEMORY;
+    }
+
     // 128-bit loads/stores need 16-byte aligned rows: ld a multiple of 16 bytes of every
     // array (ld % 4 == 0 for fp32, ld % 8 == 0 for bf16 inputs) and aligned bases.
     bool vec16 = (p.ld % (int64_t)(16 / in_elem)) == 0 && aligned(p.term, 4) &&
@@ -113,7 +166,7 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
 
     // The warp-streaming kernel moves chunks with 16-byte bulk copies: every base
     // 16-byte aligned, ld and T multiples of 16, and packed rows contiguous (ld == T).
-    bool streamable = in_elem == 4 && vec16 && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
+    bool streamable = in_elem == 4 && !p.host && vec16 && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
                       (p.T > rlca::kWarpChunk || p.ld == p.T) && aligned(p.term, 16) &&
                       (!p.trunc || aligned(p.trunc, 16));
 
@@ -327,6 +380,7 @@ const char *rlca_status_string(int status)
     case RLCA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
     case RLCA_ERR_LAUNCH: return "CUDA call failed";
     case RLCA_ERR_TIMEOUT: return "a bounded cross-block wait timed out";
+    case RLCA_ERR_MEMORY: return "a buffer is neither current-device memory nor pinned host memory";
     default: return "unknown status";
     }
 }

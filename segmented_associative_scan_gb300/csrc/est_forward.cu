@@ -53,7 +53,7 @@ cudaError_t launch_forward_typed(const Params &p_in, int vec, cudaStream_t strea
     const bool trunc = p.trunc != nullptr;
     // 128-bit access where a CTA tile holds one row (measured faster there, 8.46 vs
     // 8.53 us at [4096, 1024]); 256-bit elsewhere when the rows allow it.
-    if (one_row_per_cta(p.T)) vec = vec < 1 ? vec : 1;
+    if (one_row_per_cta(p.T) && !p.host) vec = vec < 1 ? vec : 1;
     return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
         return launch_forward_variant<decltype(v)::value, decltype(r)::value, TIn>(p, stream);
     });

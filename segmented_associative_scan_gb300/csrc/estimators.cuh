@@ -70,6 +70,7 @@ struct Params {
     int spin_limit;   // consecutive empty polls of a later tile before giving up
     int stall;        // testing only: nonzero = tiles never publish their state
     int forward;      // host-side only: a forward scan (truncation needs no values)
+    int host;         // host-side only: some data live in pinned host memory
     MultiLambda multi;  // fused TD(lambda) only
 };
 

@@ -87,13 +87,16 @@ inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 // estimator but GAE with truncation: there the dependent load of the truncation values
 // stalls a whole CTA, and the barrier-free warp-streaming kernel is 8% faster (14.7 vs
 // 16.1 us at [4096, 1024]); without truncation the CTA kernel is 6% faster (12.7 vs
-// 13.5 us). Longer rows loop over CTA tiles (or use look-back with a workspace).
+// 13.5 us). Longer rows loop over CTA tiles (or use look-back with a workspace). Data in
+// pinned host memory never take the bulk-copy kernel; GAE then uses CTA tiles (a GAE
+// step at [4096, 1024] over NVLink-C2C: 275 us, at 335 GB/s).
 template <Est E>
-inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool trunc)
+inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool trunc,
+                        bool host)
 {
     if (T > kTile) return lookback && lookback_pays(N) ? Path::kLookback : Path::kCtaRowLoop;
     if (T <= 32 * kItems) return Path::kWarpRows;
-    if (E == Est::kGae && (trunc || 2 * T <= kTile))
+    if (E == Est::kGae && (trunc || 2 * T <= kTile) && !host)
         return streamable ? Path::kWarpStream : Path::kWarpRows;
     return Path::kCtaRows;
 }
@@ -202,7 +205,9 @@ cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
 // ------------------------------------------------------------------ dispatch
 
 // Access widths. Rows that allow 256-bit access (32-byte aligned, access level 2) use
-// 256-bit loads and stores (kWideVec) unless measured slower. Measured on GB300, 128-bit
+// 256-bit loads and stores (kWideVec) unless measured slower. Data in pinned host memory
+// always take the wide access when aligned: over NVLink-C2C it moved a GAE step at 335
+// GB/s against 195 GB/s with 128-bit access. Measured on GB300 in device memory, 128-bit
 // vs 256-bit loads and stores, in us per launch:
 //   warp-owned rows [4096, 128]: return 2.23 vs 2.14, TD(lambda) 2.36 vs 2.26, V-trace
 //     3.86 vs 3.48, Retrace 3.37 vs 2.52, GAE 2.97 vs 2.51, fused TD 4.21 vs 3.93;
@@ -260,8 +265,9 @@ cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stre
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
     // bf16 data loads stay 128-bit; wide flag loads and output stores were measured
-    // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout.
-    vec = vec < 1 ? vec : 1;
+    // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout
+    // in device memory.
+    if (!p.host) vec = vec < 1 ? vec : 1;
     if (E == Est::kGae && p.T > 32 * kItems) {
         // 16 steps per lane: beta^16 for the per-lane composite.
         p.beta_pow = p.gamma_lambda;
@@ -290,12 +296,12 @@ cudaError_t launch_estimator(const Params &p_in, int vec, bool streamable, cudaS
     Params p = p_in;
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
-    const Path path = choose_path<E>(p.N, p.T, streamable, p.ws != nullptr, trunc);
+    const Path path = choose_path<E>(p.N, p.T, streamable, p.ws != nullptr, trunc, p.host);
     if (path == Path::kWarpStream)
         return trunc ? launch_warp_stream<E, true>(p, stream)
                      : launch_warp_stream<E, false>(p, stream);
     if ((E == Est::kTdLambda || E == Est::kRetrace) && path == Path::kCtaRows &&
-        one_row_per_cta(p.T))
+        one_row_per_cta(p.T) && !p.host)
         vec = vec < 1 ? vec : 1;
     return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
         return launch_path<E, decltype(v)::value, decltype(r)::value>(p, path, stream);

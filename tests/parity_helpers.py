@@ -57,7 +57,10 @@ class Placed:
 
     def __init__(self, a: np.ndarray | None, N, T, ld, offset, dtype, fill, device):
         n_el = GUARD + offset + max(N * ld, 1) + GUARD
-        self.buf = torch.full((n_el,), fill, dtype=dtype, device=device)
+        if device == "pinned":  # page-locked host memory, read and written in place
+            self.buf = torch.full((n_el,), fill, dtype=dtype).pin_memory()
+        else:
+            self.buf = torch.full((n_el,), fill, dtype=dtype, device=device)
         self.lo = GUARD + offset
         self.view = self.buf[self.lo:self.lo + N * ld].view(N, ld)[:, :T]
         if a is not None:
@@ -73,28 +76,35 @@ class Placed:
 
 def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0",
             check_guards=True, drop_second_output=False, workspace=None,
-            in_dtype=torch.float32):
+            in_dtype=torch.float32, host=None):
     """Run `est` on the CUDA path; returns {output name: float64 array}. `workspace`
     (a zeroed uint8 CUDA tensor) selects the look-back (_ex) entry point; in_dtype
-    torch.bfloat16 places the data inputs as bf16 (the _bf16 entry points)."""
+    torch.bfloat16 places the data inputs as bf16 (the _bf16 entry points). `host`
+    ("all", "inputs" or "outputs") places those buffers in pinned host memory, which
+    the kernels then read or write in place."""
     N, T = ro.N, ro.T
+    in_dev = "pinned" if host in ("all", "inputs") else device
+    out_dev = "pinned" if host in ("all", "outputs") else device
     ws = dict(workspace=workspace)
     ld = T if ld is None else ld
     p = dict(DEFAULT_PARAMS[est], **params)
 
     def f32(a):
-        return None if a is None else Placed(a, N, T, ld, offset, in_dtype, 0.0, device)
+        return None if a is None else Placed(a, N, T, ld, offset, in_dtype, 0.0, in_dev)
 
     def flag(a):
         if a is None:
             return None
         dt = torch.bool if bool_flags else torch.uint8
-        return Placed(a.astype(bool) if bool_flags else a, N, T, ld, offset, dt, 1, device)
+        return Placed(a.astype(bool) if bool_flags else a, N, T, ld, offset, dt, 1, in_dev)
 
-    boot = None if ro.bootstrap is None else torch.from_numpy(ro.bootstrap).to(device)
+    boot = None
+    if ro.bootstrap is not None:
+        boot = torch.from_numpy(ro.bootstrap)
+        boot = boot.pin_memory() if in_dev == "pinned" else boot.to(device)
     r, term, trunc = f32(ro.reward), flag(ro.terminated), flag(ro.truncated)
     tv = f32(ro.trunc_value) if ro.truncated is not None else None
-    outs = {name: Placed(None, N, T, ld, offset, torch.float32, SENTINEL, device)
+    outs = {name: Placed(None, N, T, ld, offset, torch.float32, SENTINEL, out_dev)
             for name in OUTPUTS[est]}
     if drop_second_output and len(outs) == 2:
         outs.pop(OUTPUTS[est][1])

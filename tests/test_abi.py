@@ -12,7 +12,7 @@ import segmented_associative_scan_gb300 as rlca
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "rlca.h")
 
-OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
+OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT, MEMORY = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
 
 @pytest.fixture(scope="module")
@@ -37,8 +37,9 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.rlca_version() >= 100
-    for code in (OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT):
+    for code in (OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT, MEMORY):
         assert lib.rlca_status_string(code)
+    assert b"pinned host memory" in lib.rlca_status_string(MEMORY)
     assert b"unknown" in lib.rlca_status_string(12345)
 
 
