@@ -103,10 +103,13 @@ NCU_TRAFFIC = {
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that decide which kernel runs and what it does: the device
+    code and launch logic (csrc/*.cuh, csrc/est_*.cu). The C-ABI validation (api.cu,
+    noalloc.cu) launches nothing itself and is left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_associative_scan_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith(".cuh") or (name.startswith("est_") and name.endswith(".cu")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
