@@ -475,24 +475,59 @@ def e2e_run(torch, rlca, ro, device, n_steps):
                               "ms_per_step": round(ms_serial / n_steps, 4)}}
 
 
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_gae_rows(ro, lo, hi):
+    """The fp64 oracle, as it stands, on rows [lo, hi) of the batch."""
+    import oracle
+    p = ro.params
+    oracle.gae(ro.reward[lo:hi], ro.value[lo:hi], ro.terminated[lo:hi], ro.truncated[lo:hi],
+               ro.trunc_value[lo:hi], ro.bootstrap[lo:hi], gamma=p["gamma"], lam=p["lam"])
+
+
+def oracle_gae_all_cores(ro, rows, pool, threads):
+    """The unchanged oracle on the first `rows` rows, split over `threads` host threads
+    (the C call releases the interpreter lock, so the slices run in parallel)."""
+    edges = np.linspace(0, rows, threads + 1).astype(int)
+    futs = [pool.submit(oracle_gae_rows, ro, a, b)
+            for a, b in zip(edges[:-1], edges[1:]) if b > a]
+    for f in futs:
+        f.result()
+
+
 def cpu_baseline(ro, seconds):
-    """The fp64 oracle as it stands, single thread, on the full batch, repeated for about
-    `seconds` of CPU time."""
+    """The fp64 oracle as it stands on the full batch, repeated for about `seconds` of
+    wall time: once on one thread, once split over every host core. The all-core figure
+    is the reported value; the single-thread one rides along."""
+    import concurrent.futures
     import oracle
     oracle.build()
-    p = ro.params
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.gae(ro.reward, ro.value, ro.terminated, ro.truncated, ro.trunc_value,
-                   ro.bootstrap, gamma=p["gamma"], lam=p["lam"])
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": round(reps * ro.N * ro.T / el, 1), "unit": UNIT, "cores": 1,
+
+    def timed(run):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return reps, el
+
+    reps1, el1 = timed(lambda: oracle_gae_rows(ro, 0, ro.N))
+    threads = host_threads()
+    with concurrent.futures.ThreadPoolExecutor(threads) as pool:
+        repsn, eln = timed(lambda: oracle_gae_all_cores(ro, ro.N, pool, threads))
+    return {"value": round(repsn * ro.N * ro.T / eln, 1), "unit": UNIT, "cores": threads,
             "kind": "oracle",
-            "sample": f"full [{ro.N},{ro.T}] GAE batch (seed 0), {reps} passes, "
-                      f"{el:.1f} s, single thread, fp64 C reverse loop"}
+            "sample": f"full [{ro.N},{ro.T}] GAE batch (seed 0), {repsn} passes in "
+                      f"{eln:.1f} s, rows split over {threads} threads, fp64 C reverse loop",
+            "single_thread": {"value": round(reps1 * ro.N * ro.T / el1, 1), "cores": 1,
+                              "sample": f"{reps1} passes in {el1:.1f} s"}}
 
 
 def gpu_arm(args, rank, world, local_rank, dist):
@@ -605,32 +640,33 @@ def gpu_arm(args, rank, world, local_rank, dist):
 # --------------------------------------------------------------------- reference arm
 
 def reference_arm(args):
-    """The fp64 CPU oracle as it stands, on this host's cores (one thread), each step a
-    bounded sample (the first rows) of the same [4096, 1024] GAE workload."""
+    """The fp64 CPU oracle as it stands, on every host core (rows split over threads),
+    each step a bounded sample (the first rows) of the same [4096, 1024] GAE workload."""
+    import concurrent.futures
     import oracle
     oracle.build()
     ro = workload_inputs("gae", N_ENVS, SEQ_LEN, seed=0)
-    p = ro.params
+    threads = host_threads()
+    pool = concurrent.futures.ThreadPoolExecutor(threads)
 
     def run(rows):
-        oracle.gae(ro.reward[:rows], ro.value[:rows], ro.terminated[:rows],
-                   ro.truncated[:rows], ro.trunc_value[:rows], ro.bootstrap[:rows],
-                   gamma=p["gamma"], lam=p["lam"])
+        oracle_gae_all_cores(ro, rows, pool, threads)
 
     t0 = time.perf_counter()
-    run(256)
-    per_row = (time.perf_counter() - t0) / 256
+    run(min(N_ENVS, 64 * threads))
+    per_row = (time.perf_counter() - t0) / min(N_ENVS, 64 * threads)
     budget = args.reference_seconds / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(N_ENVS, budget / max(per_row, 1e-9))))
+    rows = int(max(threads, min(N_ENVS, budget / max(per_row, 1e-9))))
     for _ in range(args.warmup):
         run(rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run(rows)
     el = time.perf_counter() - t0
+    pool.shutdown()
     value = rows * SEQ_LEN * args.steps / el
-    sample = (f"first {rows} of {N_ENVS} envs x {SEQ_LEN} steps per step, "
-              f"single thread, fp64 C reverse loop")
+    sample = (f"first {rows} of {N_ENVS} envs x {SEQ_LEN} steps per step, rows split "
+              f"over {threads} threads, fp64 C reverse loop")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -639,8 +675,8 @@ def reference_arm(args):
         "data": "synthetic: seeded rollouts with the workload's distributions (no dataset)",
         "config": {"workload": WORKLOAD, "estimator": "gae", "num_envs": N_ENVS,
                    "seq_len": SEQ_LEN, "sample_envs": rows},
-        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
