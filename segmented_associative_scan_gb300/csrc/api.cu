@@ -164,10 +164,10 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
     for (int o = 0; o < n_out; ++o) vec32 = vec32 && (!outs[o] || aligned(outs[o], 32));
     const int vec = vec32 ? 2 : (vec16 ? 1 : 0);
 
-    // The warp-streaming kernel moves chunks with 16-byte bulk copies: every base
-    // 16-byte aligned, ld and T multiples of 16, and packed rows contiguous (ld == T).
+    // The warp-streaming kernel moves chunks of rows longer than one warp chunk with
+    // 16-byte bulk copies: every base 16-byte aligned, ld and T multiples of 16.
     bool streamable = in_elem == 4 && !p.host && vec16 && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
-                      (p.T > rlca::kWarpChunk || p.ld == p.T) && aligned(p.term, 16) &&
+                      p.T > rlca::kWarpChunk && aligned(p.term, 16) &&
                       (!p.trunc || aligned(p.trunc, 16));
 
     const cudaError_t err = launch(p, vec, streamable, static_cast<cudaStream_t>(stream));

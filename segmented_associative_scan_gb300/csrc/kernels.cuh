@@ -31,7 +31,7 @@
 
 namespace rlca {
 
-enum class Tiling : int { kRows = 0, kRowLoop = 1, kLookback = 2, kWarp = 3, kRow = 4 };
+enum class Tiling : int { kRows = 0, kRowLoop = 1, kLookback = 2, kRow = 4 };
 
 template <int NT>
 struct ScanSmem {
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
     }
 }
 
-// ----------------------------------------------------------- warp-owned rows (kWarp)
+// ------------------------------------------------------------------ warp-owned rows
 
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
 // aggregates, a warp suffix scan, and the chunk's carry-in (A at the step after the

@@ -187,14 +187,11 @@ cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
         limit = sms * (per_sm > 0 ? per_sm : 1);
         WarpStreamConfig<E, TRUNC>::grid_limit[dev].store(limit, std::memory_order_relaxed);
     }
-    if (p.T <= kWarpChunk) {
-        p.segs = 1;
-        p.rows_per_tile = kWarpChunk / p.T;
-    } else {
-        p.segs = (p.T + kWarpChunk - 1) / kWarpChunk;
-        p.rows_per_tile = 1;
-    }
-    const int64_t units = p.segs == 1 ? (p.N + p.rows_per_tile - 1) / p.rows_per_tile : p.N;
+    // Rows longer than one warp chunk (the dispatch sends shorter rows to warp-owned
+    // rows): each warp walks whole rows chunk by chunk.
+    p.segs = (p.T + kWarpChunk - 1) / kWarpChunk;
+    p.rows_per_tile = 1;
+    const int64_t units = p.N;
     const int64_t warps = (int64_t)limit * kWarpsPerCta;
     const int64_t per_warp = (units + warps - 1) / warps;  // equal shares, one apart at most
     const int64_t used = (units + per_warp - 1) / per_warp;

@@ -1,11 +1,9 @@
 // Warp-owned rows with a per-warp TMA pipeline (the warp-streaming tiling).
 //
-// Every warp of a persistent grid owns a contiguous, balanced range of jobs and needs no
-// other warp: no CTA barrier and no shared scan state. A job is one chunk of
-// WCH = 32 * ITEMS steps:
-//   packed rows (T <= WCH, ld == T): rows_per_tile whole rows, contiguous in memory;
-//   row chunks  (T > WCH): the warp walks each of its rows in segs chunks from the last
-//               to the first, carrying A between them in a register.
+// Every warp of a persistent grid owns a contiguous, balanced range of rows and needs no
+// other warp: no CTA barrier and no shared scan state. It walks each of its rows in
+// chunks of WCH = 32 * ITEMS steps from the last to the first, carrying A between them
+// in a register (rows are longer than one chunk: shorter rows take warp-owned rows).
 // Lane 0 keeps STAGES chunks in flight with cp.async.bulk copies into the warp's own ring
 // of shared-memory stages (one mbarrier per stage); the whole warp scans the current
 // chunk from shared memory meanwhile: lane aggregates, a 5-round shuffle suffix scan,
@@ -40,18 +38,10 @@ struct WarpCursor {
 __device__ __forceinline__ StreamJob warp_job(const Params &p, WarpCursor c)
 {
     StreamJob j;
-    if (p.segs == 1) {
-        j.row = c.unit * p.rows_per_tile;
-        const int64_t nrows = min((int64_t)p.rows_per_tile, p.N - j.row);
-        j.src = j.row * p.T;
-        j.t_start = 0;
-        j.len = (int)(nrows * p.T);
-    } else {
-        j.row = c.unit;
-        j.t_start = c.chunk * kWarpChunk;
-        j.src = j.row * p.ld + j.t_start;
-        j.len = min(kWarpChunk, p.T - j.t_start);
-    }
+    j.row = c.unit;
+    j.t_start = c.chunk * kWarpChunk;
+    j.src = j.row * p.ld + j.t_start;
+    j.len = min(kWarpChunk, p.T - j.t_start);
     return j;
 }
 
@@ -78,8 +68,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_stream_kernel(const Pa
     unsigned char *ring = rings + w * (STAGES * L::kBytes);
     uint64_t *full = bars[w];
 
-    const bool packed = p.segs == 1;
-    const int64_t units = packed ? (p.N + p.rows_per_tile - 1) / p.rows_per_tile : p.N;
+    const int64_t units = p.N;
     const int64_t G = (int64_t)gridDim.x * WARPS;
     const int64_t g = (int64_t)blockIdx.x * WARPS + w;
     const int64_t u0 = units * g / G;
@@ -118,20 +107,15 @@ __global__ void __launch_bounds__(32 * WARPS) credit_warp_stream_kernel(const Pa
         const StreamJob j = warp_job(p, cons);
         const int li = lane * ITEMS;
         const bool active = li < j.len;
-        int64_t row = j.row;
-        int t0 = j.t_start + li;
-        if (packed) {
-            const int local_row = li / p.T;
-            row += local_row;
-            t0 = li - local_row * p.T;
-        }
+        const int64_t row = j.row;
+        const int t0 = j.t_start + li;
         Chunk<ITEMS> c;
         load_chunk_stage<E, ITEMS, TRUNC, L>(p, ring + s * L::kBytes, j, li, row, t0, active, c);
         if (!arrived) {  // the copy never completed: mark this chunk's outputs invalid
 #pragma unroll
             for (int i = 0; i < ITEMS; ++i) c.r[i] = __int_as_float(0x7fc00000);
         }
-        const float carry_in = (packed || cons.chunk == p.segs - 1) ? 0.f : carry;
+        const float carry_in = cons.chunk == p.segs - 1 ? 0.f : carry;
 
         Affine e[ITEMS];
         build<E, ITEMS>(p, row, t0, c, e);
