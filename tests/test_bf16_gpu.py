@@ -40,6 +40,21 @@ def test_bf16_layouts(ld_extra, offset):
                       run_oracle(est, ro, {}), f"{est} bf16 ld+{ld_extra} off={offset}")
 
 
+@pytest.mark.parametrize("trunc", [True, False])
+@pytest.mark.parametrize("ld_extra,offset", [(0, 0), (16, 0), (16, 8)])
+@pytest.mark.parametrize("T", [272, 512, 768, 1024])
+def test_bf16_gae_rows(T, ld_extra, offset, trunc):
+    """bf16 GAE on rows of 257-1024 steps (warp-owned rows, 16 steps per lane), with
+    and without truncation, on padded and offset layouts."""
+    ro = bf16_rounded(sr.generic(40, T, seed=T + ld_extra + offset, p_term=0.01,
+                                 p_trunc=0.005 if trunc else 0.0))
+    if not trunc:
+        ro.truncated = None
+    assert_parity(run_gpu("gae", ro, {}, ld=T + ld_extra, offset=offset,
+                          in_dtype=torch.bfloat16),
+                  run_oracle("gae", ro, {}), f"gae bf16 T={T} ld+{ld_extra} off={offset}")
+
+
 def test_bf16_workloads():
     for est, ro, p in (("gae", sr.gae_trunc(), dict(gamma=0.995, lam=0.95)),
                        ("vtrace", sr.vtrace(), dict(gamma=0.99, lam=1.0)),
