@@ -143,6 +143,16 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 
 // ------------------------------------------------------------------ warp paths
 
+// CTAs per SM the warp-owned-rows kernel asks the register allocator to fit. V-trace's
+// needs 86 registers (5 CTAs per SM); capped at 7 per SM (72 registers, 28 bytes of
+// spill) it ran 9% faster on [8192, 256] (9.18 vs 10.08 us). Retrace gained under 1%,
+// GAE lost 3%.
+template <Est E, typename TIn, int ITEMS>
+constexpr int warp_min_blocks()
+{
+    return (E == Est::kVtrace && std::is_same<TIn, float>::value && ITEMS == kItems) ? 7 : 1;
+}
+
 template <Est E, int VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
 cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 {
@@ -161,8 +171,9 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
         jobs = p.N;
     }
     const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(credit_warp_kernel<E, ITEMS, VEC, TRUNC, kWarpsPerCta, TIn>, grid,
-                      32 * kWarpsPerCta, 0, stream, p);
+    return launch_pdl(credit_warp_kernel<E, ITEMS, VEC, TRUNC, kWarpsPerCta, TIn,
+                                         warp_min_blocks<E, TIn, ITEMS>()>,
+                      grid, 32 * kWarpsPerCta, 0, stream, p);
 }
 
 // Per-device grid limit (SMs x resident CTAs) of the warp-streaming kernel.
