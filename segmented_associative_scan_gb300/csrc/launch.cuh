@@ -103,13 +103,16 @@ inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool t
 
 // ------------------------------------------------------------------ CTA tile paths
 
-// CTAs per SM the one-row tile asks the register allocator to fit. V-trace's tile needs
-// 74 registers (6 CTAs per SM); capped at 71 (7 per SM, no spills) it ran 4.8% faster
-// at [4096, 1024] (15.95 vs 16.75 us). Caps gained nothing for the other estimators.
-template <Est E, typename TIn>
-constexpr int row_min_blocks()
+// CTAs per SM the CTA tiles ask the register allocator to fit. V-trace's tiles need
+// 74-96 registers (5-6 CTAs per SM); capped they ran faster: one row per CTA at 7 per
+// SM 15.95 vs 16.75 us at [4096, 1024]; packed rows at 7 per SM 16.17 vs 16.87 us at
+// [8192, 512]; the row loop at 6 per SM 28.33 vs 31.39 us at [2048, 4096]. Caps gained
+// nothing (or lost) for the other estimators.
+template <Est E, typename TIn, Tiling TL>
+constexpr int cta_min_blocks()
 {
-    return (E == Est::kVtrace && std::is_same<TIn, float>::value) ? 7 : 1;
+    if (E != Est::kVtrace || !std::is_same<TIn, float>::value) return 1;
+    return TL == Tiling::kRowLoop ? 6 : (TL == Tiling::kLookback ? 1 : 7);
 }
 
 template <Est E, int VEC, bool TRUNC, typename TIn = float>
@@ -123,11 +126,11 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
         const unsigned grid = (unsigned)((p.N + p.rows_per_tile - 1) / p.rows_per_tile);
         if (p.rows_per_tile == 1)
             return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRow,
-                                                 row_min_blocks<E, TIn>(), TIn>,
+                                                 cta_min_blocks<E, TIn, Tiling::kRow>(), TIn>,
                               grid, kThreads, 0, stream, p);
-        return launch_pdl(
-            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows, 1, TIn>, grid,
-            kThreads, 0, stream, p);
+        return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRows,
+                                             cta_min_blocks<E, TIn, Tiling::kRows>(), TIn>,
+                          grid, kThreads, 0, stream, p);
     }
     p.chunks_per_row = kTile / kItems;
     p.rows_per_tile = 1;
@@ -136,9 +139,9 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
         return launch_pdl(
             credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback, 1, TIn>,
             (unsigned)(p.N * p.segs), kThreads, 0, stream, p);
-    return launch_pdl(
-        credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop, 1, TIn>,
-        (unsigned)p.N, kThreads, 0, stream, p);
+    return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop,
+                                         cta_min_blocks<E, TIn, Tiling::kRowLoop>(), TIn>,
+                      (unsigned)p.N, kThreads, 0, stream, p);
 }
 
 // ------------------------------------------------------------------ warp paths
