@@ -358,8 +358,10 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
 //   first with the carry in a register.
 // All warps of a typical launch are resident at once, so each keeps its next chunk's
 // loads in flight without any cross-warp wait.
+// MINB: CTAs per SM the register allocator must fit (0 = no request; an explicit 1
+// changes the allocation, so 0 is the default).
 template <Est E, int ITEMS, int VEC, bool TRUNC, int WARPS = 4, typename TIn = float,
-          int MINB = 1>
+          int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Params p)
 {
     grid_dependency_sync();

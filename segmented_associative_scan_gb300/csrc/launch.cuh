@@ -103,7 +103,10 @@ inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool t
 
 // ------------------------------------------------------------------ CTA tile paths
 
-// CTAs per SM the CTA tiles ask the register allocator to fit. V-trace's tiles need
+// CTAs per SM the CTA tiles ask the register allocator to fit. The tiles were tuned with
+// an explicit 1: leaving the request out gives fewer registers but made Retrace's row
+// loop 2.3% slower (28.23 vs 27.58 us at [2048, 4096]) and changed nothing else
+// measurably. V-trace's tiles need
 // 74-96 registers (5-6 CTAs per SM); capped they ran faster: one row per CTA at 7 per
 // SM 15.95 vs 16.75 us at [4096, 1024]; packed rows at 7 per SM 16.17 vs 16.87 us at
 // [8192, 512]; the row loop at 6 per SM 28.33 vs 31.39 us at [2048, 4096]. Caps gained
@@ -137,7 +140,8 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
     p.segs = (p.T + kTile - 1) / kTile;
     if (path == Path::kLookback)
         return launch_pdl(
-            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback, 1, TIn>,
+            credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kLookback,
+                               cta_min_blocks<E, TIn, Tiling::kLookback>(), TIn>,
             (unsigned)(p.N * p.segs), kThreads, 0, stream, p);
     return launch_pdl(credit_scan_kernel<E, kThreads, kItems, VEC, TRUNC, Tiling::kRowLoop,
                                          cta_min_blocks<E, TIn, Tiling::kRowLoop>(), TIn>,
@@ -146,14 +150,13 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 
 // ------------------------------------------------------------------ warp paths
 
-// CTAs per SM the warp-owned-rows kernel asks the register allocator to fit. V-trace's
-// needs 86 registers (5 CTAs per SM); capped at 7 per SM (72 registers, 28 bytes of
-// spill) it ran 9% faster on [8192, 256] (9.18 vs 10.08 us). Retrace gained under 1%,
-// GAE lost 3%.
+// CTAs per SM the warp-owned-rows kernel asks the register allocator to fit (0 = no
+// request). V-trace's needs 80 registers (6 CTAs per SM); capped at 7 per SM (72
+// registers, 28 bytes of spill) it ran faster on [8192, 256]: 9.16 us against 9.72.
 template <Est E, typename TIn, int ITEMS>
 constexpr int warp_min_blocks()
 {
-    return (E == Est::kVtrace && std::is_same<TIn, float>::value && ITEMS == kItems) ? 7 : 1;
+    return (E == Est::kVtrace && std::is_same<TIn, float>::value && ITEMS == kItems) ? 7 : 0;
 }
 
 template <Est E, int VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
