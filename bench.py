@@ -345,32 +345,61 @@ def n_sets_for(bytes_per_set):
     return min(64, max(3, int(np.ceil(2.5 * L2_BYTES / bytes_per_set))))
 
 
+def time_workload(torch, rlca, device, peak, est, ro):
+    """One estimator alone on the batch `ro` (copies of it rotating past L2 when it is
+    large enough): µs per launch, achieved GB/s and the roofline fractions."""
+    params = est_params(est, ro)
+    nbytes = algorithmic_bytes(est, ro)
+    base = DeviceSet(ro, device, torch.bfloat16 if est.endswith("_bf16") else None)
+    n_sets = n_sets_for(nbytes)
+    sets = [base] + [base.clone() for _ in range(n_sets - 1)]
+    for i in range(3):
+        launch(rlca, est, sets[i % len(sets)], params)
+    G = 10 * len(sets)
+    g = capture(torch, rlca, est, sets, params, G)
+    g.replay()
+    reps = max(1, 300 // G)
+    ms = timed_replay(torch, [g] * reps)
+    us = 1000.0 * ms / (G * reps)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    out = {"us_per_launch": round(us, 3), "algorithmic_bytes": nbytes,
+           "bytes_per_step": round(nbytes / (ro.N * ro.T), 3),
+           "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+           "frac_of_8tbs": round(gbs / 8000.0, 4),
+           "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1),
+           "inputs_exceed_l2": n_sets * nbytes > L2_BYTES}
+    del sets, base, g
+    torch.cuda.empty_cache()
+    return out
+
+
 def per_estimator_roofline(torch, rlca, device, peak):
     """Each estimator alone at [4096, 1024] on its own workload's distributions."""
+    return {est: time_workload(torch, rlca, device, peak, est,
+                               workload_inputs(est, N_ENVS, SEQ_LEN, seed=100))
+            for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi",
+                        "trace", "prefix_sum", "gae_bf16")}
+
+
+# The workload configurations, each at its own shape and distributions.
+CONFIGS = (
+    ("gae_16x128", "gae", 16, 128),
+    ("return_4096x128", "return", 4096, 128),
+    ("td_lambda_0.9_4096x128", "td_lambda", 4096, 128),
+    ("td_lambda_fused_0_0.9_1_4096x128", "td_multi", 4096, 128),
+    ("gae_trunc_4096x1024", "gae", 4096, 1024),
+    ("vtrace_8192x256", "vtrace", 8192, 256),
+    ("retrace_2048x4096", "retrace", 2048, 4096),
+)
+
+
+def per_config(torch, rlca, device, peak):
+    """Every workload configuration timed alone at its own shape."""
     out = {}
-    for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi", "trace",
-                "prefix_sum", "gae_bf16"):
-        ro = workload_inputs(est, N_ENVS, SEQ_LEN, seed=100)
-        params = est_params(est, ro)
-        nbytes = algorithmic_bytes(est, ro)
-        base = DeviceSet(ro, device, torch.bfloat16 if est.endswith("_bf16") else None)
-        sets = [base] + [base.clone() for _ in range(n_sets_for(nbytes) - 1)]
-        for i in range(3):
-            launch(rlca, est, sets[i % len(sets)], params)
-        G = 10 * len(sets)
-        g = capture(torch, rlca, est, sets, params, G)
-        g.replay()
-        reps = max(1, 300 // G)
-        ms = timed_replay(torch, [g] * reps)
-        us = 1000.0 * ms / (G * reps)
-        gbs = nbytes / (us * 1e-6) / 1e9
-        out[est] = {"us_per_launch": round(us, 3), "algorithmic_bytes": nbytes,
-                    "bytes_per_step": round(nbytes / (ro.N * ro.T), 3),
-                    "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                    "frac_of_8tbs": round(gbs / 8000.0, 4),
-                    "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1)}
-        del sets, base, g
-        torch.cuda.empty_cache()
+    for name, est, N, T in CONFIGS:
+        ro = sr.gae_small(N=N, T=T, seed=100) if name == "gae_16x128" else \
+            workload_inputs(est, N, T, seed=100)
+        out[name] = time_workload(torch, rlca, device, peak, est, ro)
     return out
 
 
@@ -632,6 +661,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.empty_cache()
     if world == 1 and not args.no_estimators and (N, T) == (N_ENVS, SEQ_LEN):
         result["estimators"] = per_estimator_roofline(torch, rlca, device, peak)
+        result["configs"] = per_config(torch, rlca, device, peak)
     if world == 1 and args.cpu_seconds > 0 and est == "gae":
         result["cpu_baseline"] = cpu_baseline(ro0, args.cpu_seconds)
     return result
