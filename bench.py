@@ -43,6 +43,8 @@ WORKLOADS = {
     "vtrace": "V-trace, fp32, num_envs=4096, seq_len=1024 (rates of the [8192,256] V-trace workload)",
     "retrace": "Retrace, fp32, num_envs=4096, seq_len=1024 (rates of the [2048,4096] Retrace workload)",
     "td_multi": "TD(lambda) for lambda in {0, 0.9, 1} fused, fp32, num_envs=4096, seq_len=1024",
+    "gae_vtrace": "GAE (lambda=0.95) and V-trace fused, fp32, num_envs=4096, seq_len=1024 "
+                  "(rates of the [8192,256] V-trace workload)",
     "gae_bf16": "GAE with truncation bootstrapping, bf16 inputs / fp32 math and outputs, "
                 "num_envs=4096, seq_len=1024",
     "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
@@ -62,6 +64,9 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
     if est == "td_multi":
         return ("credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)" if T <= 1024
                 else "credit_td_multi_kernel (CTA row loop, 3 lambdas per load)")
+    if est == "gae_vtrace":
+        return ("credit_gae_vtrace_kernel (CTA tiles, GAE and V-trace per load)" if T <= 1024
+                else "credit_gae_vtrace_kernel (CTA row loop, GAE and V-trace per load)")
     name = _EST_NAME[est]
     if est == "gae_bf16":
         return (f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)" if T <= 256
@@ -131,9 +136,9 @@ def algorithmic_bytes(est: str, ro) -> int:
     bootstrap values once) and every output written once."""
     n = ro.N * ro.T
     f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
-              "prefix_sum": 1, "td_multi": 2, "gae_bf16": 2}[est]
+              "prefix_sum": 1, "td_multi": 2, "gae_bf16": 2, "gae_vtrace": 3}[est]
     outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
-            "prefix_sum": 1, "td_multi": 3, "gae_bf16": 2}[est]
+            "prefix_sum": 1, "td_multi": 3, "gae_bf16": 2, "gae_vtrace": 4}[est]
     in_bytes = 2 if est.endswith("_bf16") else 4
     b = n * (in_bytes * f32_in + 1 + 4 * outs)
     if ro.truncated is not None:
@@ -153,7 +158,7 @@ def workload_inputs(est: str, N: int, T: int, seed: int):
         return sr.traces(N=N, T=T, seed=seed)
     if est in ("return", "td_lambda", "td_multi"):
         return sr.return_td(N=N, T=T, seed=seed)
-    if est == "vtrace":
+    if est in ("vtrace", "gae_vtrace"):
         return sr.vtrace(N=N, T=T, seed=seed)
     return sr.retrace(N=N, T=T, seed=seed)
 
@@ -266,7 +271,7 @@ class DeviceSet:
         self.log_rho, self.q_taken, self.expected_q, self.rho = (
             t(ro.log_rho), t(ro.q_taken), t(ro.expected_q), t(ro.rho))
         z = lambda: torch.empty((ro.N, ro.T), dtype=torch.float32, device=device)
-        self.out0, self.out1, self.out2 = z(), z(), z()
+        self.out0, self.out1, self.out2, self.out3 = z(), z(), z(), z()
         self.ws = None  # look-back workspace (the _ex entry points), when asked for
 
     def clone(self):
@@ -300,6 +305,12 @@ def launch(rlca, est, s, params):
         rlca.rlca_retrace(s.reward, s.q_taken, s.expected_q, s.rho, **fl,
                           bootstrap_ev=s.bootstrap, gamma=g, lam=params["lam"], q_ret=s.out0,
                           workspace=ws)
+    elif est == "gae_vtrace":
+        rlca.rlca_gae_vtrace(s.reward, s.value, s.log_rho, **fl, bootstrap=s.bootstrap, gamma=g,
+                             lam=0.95, lam_vtrace=params["lam"], rho_bar=params["rho_bar"],
+                             c_bar=params["c_bar"], pg_rho_bar=params["pg_rho_bar"],
+                             advantages=s.out0, returns=s.out1, vs=s.out2,
+                             pg_advantages=s.out3)
     elif est == "td_multi":
         rlca.rlca_td_lambda_multi(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
                                   lams=params["lams"], targets=[s.out0, s.out1, s.out2])
@@ -378,7 +389,7 @@ def per_estimator_roofline(torch, rlca, device, peak):
     return {est: time_workload(torch, rlca, device, peak, est,
                                workload_inputs(est, N_ENVS, SEQ_LEN, seed=100))
             for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi",
-                        "trace", "prefix_sum", "gae_bf16")}
+                        "gae_vtrace", "trace", "prefix_sum", "gae_bf16")}
 
 
 # The workload configurations, each at its own shape and distributions.

@@ -169,6 +169,22 @@ int rlca_td_lambda_multi(const float *reward, const float *value, const uint8_t 
                          float *const *targets, void *stream);
 
 /*
+ * GAE and V-trace in one pass (fused): reward, value, log_rho and the flags are read from
+ * HBM once; both estimators are scanned on chip and their four outputs written once
+ * (Method section 2: the load, not the arithmetic, is what costs). The outputs equal
+ * rlca_gae with lambda_gae (advantages, returns) and rlca_vtrace with lambda_vtrace,
+ * rho_bar, c_bar, pg_rho_bar (vs, pg_advantages), for the same value estimates.
+ * advantages and vs are required; returns and pg_advantages are nullable (not written).
+ * No output may overlap an input or another output.
+ */
+int rlca_gae_vtrace(const float *reward, const float *value, const float *log_rho,
+                    const uint8_t *terminated, const uint8_t *truncated,
+                    const float *trunc_value, const float *bootstrap, float gamma,
+                    float lambda_gae, float lambda_vtrace, float rho_bar, float c_bar,
+                    float pg_rho_bar, int64_t N, int64_t T, int64_t ld, float *advantages,
+                    float *returns, float *vs, float *pg_advantages, void *stream);
+
+/*
  * Forward-time scans (Method section 1: eligibility traces are the forward-time mirror
  * of the recurrence; episodic prefix sums are among the estimators it covers).
  *   A_t = x_t + decay * A_{t-1} inside an episode; A_t = x_t at a step whose previous

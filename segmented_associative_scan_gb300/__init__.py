@@ -45,6 +45,8 @@ SIGNATURES = {
                      ctypes.c_int),
     "rlca_td_lambda_multi": ([_P, _P, _P, _P, _P, _P, _F, _P, ctypes.c_int, _I64, _I64, _I64,
                               _P, _P], ctypes.c_int),
+    "rlca_gae_vtrace": ([_P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _F, _F, _I64, _I64, _I64,
+                         _P, _P, _P, _P, _P], ctypes.c_int),
     "rlca_eligibility_trace": ([_P, _P, _P, _P, _F, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "rlca_episodic_prefix_sum": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "rlca_workspace_bytes": ([_I64, _I64], ctypes.c_size_t),
@@ -280,6 +282,32 @@ def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=
     return vs, pg
 
 
+def rlca_gae_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=None,
+                    bootstrap=None, gamma=0.99, lam=0.95, lam_vtrace=1.0, rho_bar=1.0,
+                    c_bar=1.0, pg_rho_bar=None, advantages=None, returns=None, vs=None,
+                    pg_advantages=None, want_returns=True, want_pg=True):
+    """GAE and V-trace from one read of the inputs (fp32): returns (advantages, returns,
+    vs, pg_advantages); returns / pg_advantages are None when not wanted."""
+    g = _Rows(reward)
+    args = (g.ptr(reward, "reward", _F32), g.ptr(value, "value", _F32),
+            g.ptr(log_rho, "log_rho", _F32), g.ptr(terminated, "terminated", _FLAG),
+            g.ptr(truncated, "truncated", _FLAG, True),
+            g.ptr(trunc_value, "trunc_value", _F32, truncated is None),
+            g.vec_ptr(bootstrap, "bootstrap"))
+    adv = g.out(advantages, "advantages")
+    ret = g.out(returns, "returns") if (want_returns or returns is not None) else None
+    vs = g.out(vs, "vs")
+    pg = g.out(pg_advantages, "pg_advantages") if (want_pg or pg_advantages is not None) \
+        else None
+    if pg_rho_bar is None:
+        pg_rho_bar = rho_bar
+    ptr = lambda t: None if t is None else (t.data_ptr() or None)
+    _check("rlca_gae_vtrace", lib().rlca_gae_vtrace(
+        *args, gamma, lam, lam_vtrace, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld, ptr(adv),
+        ptr(ret), ptr(vs), ptr(pg), _stream(g.device)))
+    return adv, ret, vs, pg
+
+
 def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
                  trunc_value=None, bootstrap_ev=None, gamma=0.99, lam=0.95, q_ret=None,
                  workspace=None):
@@ -350,6 +378,7 @@ discounted_return = rlca_discounted_return
 td_lambda = rlca_td_lambda
 gae = rlca_gae
 vtrace = rlca_vtrace
+gae_vtrace = rlca_gae_vtrace
 retrace = rlca_retrace
 td_lambda_multi = rlca_td_lambda_multi
 eligibility_trace = rlca_eligibility_trace

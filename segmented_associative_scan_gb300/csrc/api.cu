@@ -307,6 +307,41 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
 }
 
+int gae_vtrace(const float *reward, const float *value, const float *log_rho,
+               const uint8_t *terminated, const uint8_t *truncated, const float *trunc_value,
+               const float *bootstrap, float gamma, float lambda_gae, float lambda_vtrace,
+               float rho_bar, float c_bar, float pg_rho_bar, int64_t N, int64_t T, int64_t ld,
+               float *advantages, float *returns, float *vs, float *pg_advantages, void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda_gae) || bad_lambda(lambda_vtrace) ||
+        bad_clip(rho_bar) || bad_clip(c_bar) || bad_clip(pg_rho_bar))
+        return RLCA_ERR_PARAM;
+    Params pv = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                            lambda_vtrace, N, T, ld);
+    pv.value = value;
+    pv.aux = log_rho;
+    pv.rho_bar = rho_bar;
+    pv.c_bar = c_bar;
+    pv.pg_rho_bar = pg_rho_bar;
+    pv.out0 = vs;
+    pv.out1 = pg_advantages;
+    Params pg = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                            lambda_gae, N, T, ld);
+    pg.value = value;
+    pg.out0 = advantages;
+    pg.out1 = returns;
+    bool empty = false;
+    if (check_shape(N, T, ld, &empty) == RLCA_OK && !empty && !advantages) return RLCA_ERR_NULL;
+    const float *in[] = {reward, value, log_rho};
+    float *out[] = {vs, advantages, returns, pg_advantages};
+    auto launch = [&pg](const Params &q, int vec, bool, cudaStream_t s) {
+        Params g = pg;  // the same validated shape and memory kind as the V-trace half
+        g.host = q.host;
+        return rlca::launch_gae_vtrace(g, q, vec, s);
+    };
+    return validate_and_launch(pv, in, 3, out, 4, Workspace{nullptr, 0}, launch, stream);
+}
+
 int td_lambda_multi(const float *reward, const float *value, const uint8_t *terminated,
                     const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
                     float gamma, const float *lambdas, int n_lambdas, int64_t N, int64_t T,
@@ -518,6 +553,18 @@ int rlca_td_lambda_multi(const float *reward, const float *value, const uint8_t 
 {
     return td_lambda_multi(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
                            lambdas, n_lambdas, N, T, ld, targets, stream);
+}
+
+int rlca_gae_vtrace(const float *reward, const float *value, const float *log_rho,
+                    const uint8_t *terminated, const uint8_t *truncated,
+                    const float *trunc_value, const float *bootstrap, float gamma,
+                    float lambda_gae, float lambda_vtrace, float rho_bar, float c_bar,
+                    float pg_rho_bar, int64_t N, int64_t T, int64_t ld, float *advantages,
+                    float *returns, float *vs, float *pg_advantages, void *stream)
+{
+    return gae_vtrace(reward, value, log_rho, terminated, truncated, trunc_value, bootstrap,
+                      gamma, lambda_gae, lambda_vtrace, rho_bar, c_bar, pg_rho_bar, N, T, ld,
+                      advantages, returns, vs, pg_advantages, stream);
 }
 
 int rlca_eligibility_trace(const float *x, const uint8_t *terminated,

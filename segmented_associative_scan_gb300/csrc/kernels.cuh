@@ -326,6 +326,43 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
     }
 }
 
+// ------------------------------------------------------ fused GAE + V-trace
+
+// GAE and V-trace from one load of a tile: the V-trace chunk (reward, value, log ratios,
+// flags) holds every input GAE reads, so the tile is loaded once and scanned twice. GAE
+// goes first: V-trace's build turns the log ratios into ratios in place. `pg` holds the
+// GAE parameters and outputs, `pv` the V-trace ones; the two scans alternate the shared
+// buffers.
+template <int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL, int MINB = 1>
+__global__ void __launch_bounds__(NT, MINB) credit_gae_vtrace_kernel(const Params pg,
+                                                                      const Params pv)
+{
+    __shared__ ScanSmem<NT> sm;
+    grid_dependency_sync();
+    constexpr int TILE = NT * ITEMS;
+    auto tile = [&](int64_t row, int t0, bool active, float (&carry)[2], int buf) {
+        Chunk<ITEMS> c;
+        load_chunk<Est::kVtrace, ITEMS, VEC, TRUNC>(pv, row, t0, active, threadIdx.x & 31, c);
+        carry[0] = scan_chunk<Est::kGae, NT, ITEMS, VEC, false>(pg, c, row, t0, carry[0], sm,
+                                                                  buf);
+        carry[1] = scan_chunk<Est::kVtrace, NT, ITEMS, VEC, false>(pv, c, row, t0, carry[1],
+                                                                     sm, buf ^ 1);
+    };
+    float carry[2] = {0.f, 0.f};
+    if (TL == Tiling::kRows) {
+        const int local_row = threadIdx.x / pv.chunks_per_row;
+        const int chunk = threadIdx.x - local_row * pv.chunks_per_row;
+        const int64_t row = (int64_t)blockIdx.x * pv.rows_per_tile + local_row;
+        tile(row, chunk * ITEMS, local_row < pv.rows_per_tile && row < pv.N, carry, 0);
+    } else if (TL == Tiling::kRow) {
+        tile(blockIdx.x, threadIdx.x * ITEMS, true, carry, 0);
+    } else {
+        const int64_t row = blockIdx.x;
+        for (int s = pv.segs - 1; s >= 0; --s)
+            tile(row, s * TILE + threadIdx.x * ITEMS, true, carry, 0);
+    }
+}
+
 // ------------------------------------------------------------------ warp-owned rows
 
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane

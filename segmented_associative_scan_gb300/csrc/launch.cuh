@@ -38,9 +38,10 @@ inline size_t workspace_bytes(int64_t N, int64_t T)
 // sleeps up to 256 ns, so about a second) before the launch reports RLCA_ERR_TIMEOUT.
 constexpr int kDefaultSpinLimit = 1 << 22;
 
-template <typename Kernel>
+// Launch with programmatic stream serialization (PDL); `args` are the kernel's Params.
+template <typename Kernel, typename... Args>
 cudaError_t launch_pdl(Kernel kernel, unsigned grid, unsigned block, size_t smem,
-                       cudaStream_t stream, const Params &p)
+                       cudaStream_t stream, const Args &...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -52,7 +53,7 @@ cudaError_t launch_pdl(Kernel kernel, unsigned grid, unsigned block, size_t smem
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ------------------------------------------------------------------ kernel choice
@@ -345,6 +346,8 @@ cudaError_t launch_vtrace_bf16(const Params &p, int vec, cudaStream_t stream);
 cudaError_t launch_retrace_bf16(const Params &p, int vec, cudaStream_t stream);
 // Fused TD(lambda) for p.multi.count lambdas (outputs in p.multi.out).
 cudaError_t launch_td_multi(const Params &p, int vec, cudaStream_t stream);
+// Fused GAE (parameters and outputs in pg) and V-trace (pv) from one load of the inputs.
+cudaError_t launch_gae_vtrace(const Params &pg, const Params &pv, int vec, cudaStream_t stream);
 // Forward scans: p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
 cudaError_t launch_forward(const Params &p, int vec, cudaStream_t stream);
 cudaError_t launch_forward_bf16(const Params &p, int vec, cudaStream_t stream);

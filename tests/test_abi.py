@@ -145,3 +145,26 @@ def test_td_lambda_multi_validation(lib):
     assert call(2, tg=same) == ALIAS
     into_input = (ctypes.c_void_p * 2)(fake(4), fake(2))
     assert call(2, tg=into_input) == ALIAS
+
+
+def gae_vtrace_args(**kw):
+    a = dict(reward=fake(1), value=fake(2), log_rho=fake(3), term=fake(4), trunc=None,
+             tv=None, boot=None, gamma=0.99, lam=0.95, lam_v=1.0, rb=1.0, cb=1.0, pb=1.0,
+             N=4, T=64, ld=64, adv=fake(5), ret=fake(6), vs=fake(7), pg=fake(8), stream=None)
+    a.update(kw)
+    return tuple(a[k] for k in ("reward", "value", "log_rho", "term", "trunc", "tv", "boot",
+                                "gamma", "lam", "lam_v", "rb", "cb", "pb", "N", "T", "ld",
+                                "adv", "ret", "vs", "pg", "stream"))
+
+
+def test_gae_vtrace_validation(lib):
+    f = lib.rlca_gae_vtrace
+    assert f(*gae_vtrace_args(adv=None)) == NULL  # both primary outputs are required
+    assert f(*gae_vtrace_args(vs=None)) == NULL
+    assert f(*gae_vtrace_args(log_rho=None)) == NULL
+    assert f(*gae_vtrace_args(N=0, reward=None, adv=None, vs=None)) == OK  # empty
+    assert f(*gae_vtrace_args(lam=1.5)) == PARAM
+    assert f(*gae_vtrace_args(lam_v=-0.5)) == PARAM
+    assert f(*gae_vtrace_args(cb=0.0)) == PARAM
+    assert f(*gae_vtrace_args(vs=fake(5))) == ALIAS  # vs on advantages
+    assert f(*gae_vtrace_args(pg=fake(3))) == ALIAS  # pg on log ratios
