@@ -91,19 +91,20 @@ L2_BYTES = 129 * 2 ** 20
 # keyed by (hash of the kernel sources at the time of the capture, estimator, N, T,
 # workspace); null once the kernels change. Within one captured launch the outputs stay
 # in L2, so these are mostly reads. Summaries with the commands: profiles/*_kernel.md.
-_H = "4b948af4f9e8e0c9"
+_H = "9b412c1b75061fdf"
 NCU_TRAFFIC = {
-    (_H, "gae", 4096, 1024, False): 43_966_720,
-    (_H, "return", 4096, 1024, False): 20_996_096,
-    (_H, "td_lambda", 4096, 1024, False): 37_783_808,
-    (_H, "vtrace", 4096, 1024, False): 57_017_600,
-    (_H, "retrace", 4096, 1024, False): 73_137_920,
-    (_H, "td_multi", 4096, 1024, False): 40_598_528,
-    (_H, "trace", 4096, 1024, False): 25_192_960,
-    (_H, "gae_bf16", 4096, 1024, False): 26_248_960,
-    (_H, "retrace", 2048, 4096, False): 158_160_384,
-    (_H, "return", 4096, 128, False): 2_650_880,
-    (_H, "return", 16, 524288, True): 43_101_696,
+    (_H, "gae", 4096, 1024, False): 44_082_688,
+    (_H, "return", 4096, 1024, False): 20_995_840,
+    (_H, "td_lambda", 4096, 1024, False): 37_785_088,
+    (_H, "vtrace", 4096, 1024, False): 57_103_104,
+    (_H, "retrace", 4096, 1024, False): 73_078_528,
+    (_H, "td_multi", 4096, 1024, False): 40_365_568,
+    (_H, "trace", 4096, 1024, False): 25_192_448,
+    (_H, "gae_bf16", 4096, 1024, False): 26_243_072,
+    (_H, "retrace", 2048, 4096, False): 157_858_304,
+    (_H, "return", 4096, 128, False): 2_651_136,
+    (_H, "return", 16, 524288, True): 43_005_184,
+    (_H, "gae_vtrace", 4096, 1024, False): 67_688_448,
 }
 
 
