@@ -158,7 +158,8 @@ int rlca_retrace(const float *reward, const float *q_taken, const float *expecte
  * HBM traffic, not arithmetic, bounds these scans, so sharing the load is what pays).
  * Each targets[k] equals rlca_td_lambda with lambdas[k] (lambda = 1 gives the discounted
  * return). lambdas: host array of n_lambdas values in [0, 1]; targets: host array of
- * n_lambdas device pointers [N, ld], none NULL, overlapping no input and no other target.
+ * n_lambdas output pointers [N, ld] (device or pinned host memory), none NULL, overlapping
+ * no input and no other target.
  * 1 <= n_lambdas <= RLCA_TD_LAMBDA_MAX, else RLCA_ERR_PARAM.
  */
 #define RLCA_TD_LAMBDA_MAX 4
