@@ -405,13 +405,74 @@ CONFIGS = (
 )
 
 
-def per_config(torch, rlca, device, peak):
-    """Every workload configuration timed alone at its own shape."""
+def oracle_rows(est, ro, lo, hi):
+    """The fp64 oracle, as it stands, for estimator `est` on rows [lo, hi)."""
+    import oracle
+    p = est_params(est, ro)
+    sl = lambda a: None if a is None else a[lo:hi]
+    fl = dict(terminated=sl(ro.terminated), truncated=sl(ro.truncated),
+              trunc_value=sl(ro.trunc_value))
+    if est == "return":
+        oracle.discounted_return(sl(ro.reward), bootstrap=sl(ro.bootstrap), **fl,
+                                 gamma=p["gamma"])
+    elif est == "td_lambda":
+        oracle.td_lambda(sl(ro.reward), sl(ro.value), bootstrap=sl(ro.bootstrap), **fl,
+                         gamma=p["gamma"], lam=p["lam"])
+    elif est == "td_multi":
+        for lam in p["lams"]:
+            oracle.td_lambda(sl(ro.reward), sl(ro.value), bootstrap=sl(ro.bootstrap), **fl,
+                             gamma=p["gamma"], lam=lam)
+    elif est == "gae":
+        oracle.gae(sl(ro.reward), sl(ro.value), bootstrap=sl(ro.bootstrap), **fl,
+                   gamma=p["gamma"], lam=p["lam"])
+    elif est == "vtrace":
+        oracle.vtrace(sl(ro.reward), sl(ro.value), sl(ro.log_rho), bootstrap=sl(ro.bootstrap),
+                      **fl, gamma=p["gamma"], lam=p["lam"], rho_bar=p["rho_bar"],
+                      c_bar=p["c_bar"], pg_rho_bar=p["pg_rho_bar"])
+    else:
+        oracle.retrace(sl(ro.reward), sl(ro.q_taken), sl(ro.expected_q), sl(ro.rho),
+                       bootstrap_ev=sl(ro.bootstrap), **fl, gamma=p["gamma"], lam=p["lam"])
+
+
+def oracle_rate(est, ro, seconds, pool=None, threads=1):
+    """Timesteps/s of the oracle on the whole batch, repeated for about `seconds`: on one
+    thread, or with rows split over `threads` threads of `pool`."""
+    def run():
+        if pool is None:
+            oracle_rows(est, ro, 0, ro.N)
+            return
+        edges = np.linspace(0, ro.N, threads + 1).astype(int)
+        futs = [pool.submit(oracle_rows, est, ro, a, b)
+                for a, b in zip(edges[:-1], edges[1:]) if b > a]
+        for f in futs:
+            f.result()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return round(reps * ro.N * ro.T / el, 1)
+
+
+def per_config(torch, rlca, device, peak, cpu_seconds):
+    """Every workload configuration timed alone at its own shape, with the fp64 oracle
+    timed beside it on one host thread and on every host core."""
+    import concurrent.futures
+    import oracle
+    oracle.build()
+    threads = host_threads()
     out = {}
-    for name, est, N, T in CONFIGS:
-        ro = sr.gae_small(N=N, T=T, seed=100) if name == "gae_16x128" else \
-            workload_inputs(est, N, T, seed=100)
-        out[name] = time_workload(torch, rlca, device, peak, est, ro)
+    with concurrent.futures.ThreadPoolExecutor(threads) as pool:
+        for name, est, N, T in CONFIGS:
+            ro = sr.gae_small(N=N, T=T, seed=100) if name == "gae_16x128" else \
+                workload_inputs(est, N, T, seed=100)
+            out[name] = time_workload(torch, rlca, device, peak, est, ro)
+            if cpu_seconds > 0:
+                out[name]["oracle_timesteps_per_s"] = {
+                    "single_thread": oracle_rate(est, ro, cpu_seconds),
+                    "all_cores": oracle_rate(est, ro, cpu_seconds, pool, threads),
+                    "cores": threads}
     return out
 
 
@@ -673,7 +734,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.empty_cache()
     if world == 1 and not args.no_estimators and (N, T) == (N_ENVS, SEQ_LEN):
         result["estimators"] = per_estimator_roofline(torch, rlca, device, peak)
-        result["configs"] = per_config(torch, rlca, device, peak)
+        result["configs"] = per_config(torch, rlca, device, peak,
+                                       min(1.0, args.cpu_seconds / 10.0))
     if world == 1 and args.cpu_seconds > 0 and est == "gae":
         result["cpu_baseline"] = cpu_baseline(ro0, args.cpu_seconds)
     return result
