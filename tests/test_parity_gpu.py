@@ -184,6 +184,18 @@ def test_access_widths(ld_extra, offset, T):
         assert_parity(g, run_oracle(est, ro, {}), f"{est} T={T} ld=T+{ld_extra} off={offset}")
 
 
+@pytest.mark.parametrize("T", [13, 250, 517, 1001, 1023, 3001])
+def test_wide_access_with_ragged_tails(T):
+    """Rows padded to a multiple of 8 floats (256-bit access) whose length is not: every
+    thread but the row's last moves its steps with wide accesses, the last one steps
+    through its tail with scalar ones."""
+    ld = (T + 7) // 8 * 8
+    ro = sr.generic(19, T, seed=T + 5, p_term=0.01, p_trunc=0.005)
+    for est in ESTIMATORS:
+        assert_parity(run_gpu(est, ro, {}, ld=ld), run_oracle(est, ro, {}),
+                      f"{est} T={T} ld={ld}")
+
+
 def test_bool_flags():
     ro = sr.generic(8, 333, seed=15, p_term=0.05, p_trunc=0.05)
     for est in ESTIMATORS:
