@@ -119,3 +119,12 @@ def test_forward_workload_sizes():
         for kind in ("trace", "sum"):
             g, r = run_both(ro, kind)
             assert_parity({"o": g}, {"o": r}, f"{kind} {N}x{T}")
+
+
+@pytest.mark.parametrize("kind", ["trace", "prefix_sum"])
+@pytest.mark.parametrize("T", [13, 250, 1001, 3001])
+def test_wide_access_with_ragged_tails(kind, T):
+    """Rows padded to a multiple of 8 floats (256-bit access) with a ragged last thread."""
+    ro = sr.generic(11, T, seed=T + 17, p_term=0.02, p_trunc=0.01)
+    got, ref = run_both(ro, kind, ld=(T + 7) // 8 * 8)
+    assert_parity({"o": got}, {"o": ref}, f"{kind} T={T}")

@@ -102,3 +102,11 @@ def test_vtrace_workload_with_gae():
 def test_pinned_host_buffers():
     ro = sr.generic(16, 1024, seed=13)
     assert_parity(run_pair(ro, P, device="pinned"), oracle_pair(ro, P), "gae+vtrace host")
+
+
+@pytest.mark.parametrize("T", [13, 250, 1001, 3001])
+def test_wide_access_with_ragged_tails(T):
+    """Rows padded to a multiple of 8 floats (256-bit access) with a ragged last thread."""
+    ro = sr.generic(11, T, seed=T + 29, p_term=0.02, p_trunc=0.01)
+    assert_parity(run_pair(ro, P, ld=(T + 7) // 8 * 8), oracle_pair(ro, P),
+                  f"gae+vtrace T={T}")

@@ -85,3 +85,15 @@ def test_full_size_4096x1024():
         ref = oracle.td_lambda(ro.reward, ro.value, ro.terminated, bootstrap=ro.bootstrap,
                                gamma=0.99, lam=lam)
         assert_parity({"t": g}, {"t": ref}, f"lambda={lam}")
+
+
+@pytest.mark.parametrize("T", [13, 250, 1001, 3001])
+def test_wide_access_with_ragged_tails(T):
+    """Rows padded to a multiple of 8 floats (256-bit access) with a ragged last thread."""
+    ro = sr.generic(11, T, seed=T + 23, p_term=0.02, p_trunc=0.01)
+    lams = [0.0, 0.9, 1.0]
+    got = run(ro, lams, ld=(T + 7) // 8 * 8)
+    for g, lam in zip(got, lams):
+        ref = oracle.td_lambda(ro.reward, ro.value, ro.terminated, ro.truncated,
+                               ro.trunc_value, ro.bootstrap, gamma=0.99, lam=lam)
+        assert_parity({"t": g}, {"t": ref}, f"td multi lambda={lam} T={T}")
