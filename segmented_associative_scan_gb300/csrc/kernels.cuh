@@ -9,10 +9,12 @@
 // combined through shared memory. Each thread then replays its own items from its
 // carry-in, so every A_t comes out of registers and is written once.
 //
-// Three tilings of the [N, T] rollout:
+// Four tilings of the [N, T] rollout:
 //   kRows      (T <= NT*ITEMS): a tile holds rows_per_tile whole rows, each padded to a
 //              multiple of ITEMS. Every row ends in a reset at t = T-1, so tiles are
 //              independent and no carry crosses a tile.
+//   kRow       (NT*ITEMS/2 < T <= NT*ITEMS): kRows with exactly one row per tile; the
+//              row and a thread's first step follow from the indices alone.
 //   kRowLoop   (T > NT*ITEMS): one CTA per row walks the row's segs tiles from the last
 //              to the first, carrying A at the first step of the later tile in registers.
 //              Only one tile is on chip at a time, so long sequences never exhaust
@@ -25,6 +27,10 @@
 //              first step) once known; a tile folds later aggregates until it meets an
 //              inclusive value. A tile whose aggregate contains a reset knows its
 //              inclusive value at once, so look-back never passes an episode boundary.
+//
+// Also here: the fused kernels (TD(lambda) for several lambdas, GAE with V-trace: one
+// load of a tile, one scan per estimator) and the warp-owned-rows kernel (a warp scans
+// whole short rows, or walks a row in warp-sized chunks, with no CTA barrier).
 #pragma once
 
 #include "estimators.cuh"
