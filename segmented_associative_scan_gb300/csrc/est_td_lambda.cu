@@ -16,6 +16,17 @@ cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream)
 template <int VEC, bool TRUNC>
 cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
 {
+    constexpr int CH = 32 * kItems;
+    if (p.T <= CH) {  // warp-owned rows: whole rows per warp, no CTA barrier
+        const int t_pad = (p.T + kItems - 1) / kItems * kItems;
+        p.chunks_per_row = t_pad / kItems;
+        p.rows_per_tile = CH / t_pad;
+        p.segs = 1;
+        const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
+        const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
+        return launch_pdl(credit_td_multi_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
+                          32 * kWarpsPerCta, 0, stream, p);
+    }
     if (p.T <= kTile) {
         const int t_pad = (p.T + kItems - 1) / kItems * kItems;
         p.chunks_per_row = t_pad / kItems;

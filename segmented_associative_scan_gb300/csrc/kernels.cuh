@@ -332,6 +332,44 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
     }
 }
 
+// Fused TD(lambda) on warp-owned rows (T <= 32 * ITEMS): each warp loads its whole rows
+// once and scans them once per lambda with shuffles only (no CTA barrier). Rows end in a
+// reset at the window end, so each lambda's scan starts from a carry of 0.
+template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4>
+__global__ void __launch_bounds__(32 * WARPS) credit_td_multi_warp_kernel(const Params p)
+{
+    grid_dependency_sync();
+    constexpr Est E = Est::kTdLambda;
+    const int lane = threadIdx.x & 31;
+    const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const int local_row = lane / p.chunks_per_row;
+    const int chunk = lane - local_row * p.chunks_per_row;
+    const int64_t row = job * p.rows_per_tile + local_row;
+    const bool active = local_row < p.rows_per_tile && row < p.N;
+    const int t0 = chunk * ITEMS;
+    Chunk<ITEMS> c;
+    load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
+#pragma unroll
+    for (int k = 0; k < kMaxLambdas; ++k) {
+        if (k < p.multi.count) {
+            Params q = p;
+            q.gamma_lambda = p.multi.gamma_lambda[k];
+            q.gamma_one_m_lambda = p.multi.gamma_one_m_lambda[k];
+            q.beta_pow = p.multi.beta_pow[k];
+            q.out0 = p.multi.out[k];
+            Affine e[ITEMS];
+            build<E, ITEMS>(q, row, t0, c, e);
+            const Affine incl = warp_suffix_scan(thread_aggregate<E, ITEMS>(q, c, e), lane);
+            Affine excl = shfl_down(incl, 1);
+            if (lane == 31) excl = affine_identity();
+            const float a_after = affine_apply(excl, 0.f);
+            float A[ITEMS];
+            replay<E, ITEMS>(q, c, e, a_after, A);
+            epilogue<E, ITEMS, VEC>(q, c, A, a_after, row, t0);
+        }
+    }
+}
+
 // ------------------------------------------------------ fused GAE + V-trace
 
 // GAE and V-trace from one load of a tile: the V-trace chunk (reward, value, log ratios,
