@@ -22,6 +22,18 @@ template <int VEC, bool TRUNC>
 cudaError_t launch_gae_vtrace_variant(Params pg, Params pv, cudaStream_t stream)
 {
     unsigned grid;
+    constexpr int CH = 32 * kItems;
+    if (pv.T <= CH) {  // warp-owned rows, capped at 6 CTAs per SM like the tiles
+        const int t_pad = (pv.T + kItems - 1) / kItems * kItems;
+        pv.chunks_per_row = t_pad / kItems;
+        pv.rows_per_tile = CH / t_pad;
+        pv.segs = 1;
+        const int64_t jobs = (pv.N + pv.rows_per_tile - 1) / pv.rows_per_tile;
+        grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
+        return launch_pdl(credit_gae_vtrace_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta,
+                                                        kPairMinBlocks>,
+                          grid, 32 * kWarpsPerCta, 0, stream, pg, pv);
+    }
     if (pv.T <= kTile) {
         const int t_pad = (pv.T + kItems - 1) / kItems * kItems;
         pv.chunks_per_row = t_pad / kItems;

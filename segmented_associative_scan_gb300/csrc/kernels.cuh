@@ -407,6 +407,48 @@ __global__ void __launch_bounds__(NT, MINB) credit_gae_vtrace_kernel(const Param
     }
 }
 
+// Fused GAE + V-trace on warp-owned rows (T <= 32 * ITEMS): each warp loads its whole
+// rows once (the V-trace chunk) and scans them for GAE, then for V-trace, with shuffles
+// only. MINB: CTAs per SM the register allocator must fit (0 = no request).
+template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4, int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_gae_vtrace_warp_kernel(
+    const Params pg, const Params pv)
+{
+    grid_dependency_sync();
+    const int lane = threadIdx.x & 31;
+    const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const int local_row = lane / pv.chunks_per_row;
+    const int chunk = lane - local_row * pv.chunks_per_row;
+    const int64_t row = job * pv.rows_per_tile + local_row;
+    const bool active = local_row < pv.rows_per_tile && row < pv.N;
+    const int t0 = chunk * ITEMS;
+    Chunk<ITEMS> c;
+    load_chunk<Est::kVtrace, ITEMS, VEC, TRUNC>(pv, row, t0, active, lane, c);
+    {
+        Affine e[ITEMS];
+        build<Est::kGae, ITEMS>(pg, row, t0, c, e);
+        const Affine incl = warp_suffix_scan(thread_aggregate<Est::kGae, ITEMS>(pg, c, e), lane);
+        Affine excl = shfl_down(incl, 1);
+        if (lane == 31) excl = affine_identity();
+        const float a_after = affine_apply(excl, 0.f);
+        float A[ITEMS];
+        replay<Est::kGae, ITEMS>(pg, c, e, a_after, A);
+        epilogue<Est::kGae, ITEMS, VEC>(pg, c, A, a_after, row, t0);
+    }
+    {
+        Affine e[ITEMS];
+        build<Est::kVtrace, ITEMS>(pv, row, t0, c, e);
+        const Affine incl =
+            warp_suffix_scan(thread_aggregate<Est::kVtrace, ITEMS>(pv, c, e), lane);
+        Affine excl = shfl_down(incl, 1);
+        if (lane == 31) excl = affine_identity();
+        const float a_after = affine_apply(excl, 0.f);
+        float A[ITEMS];
+        replay<Est::kVtrace, ITEMS>(pv, c, e, a_after, A);
+        epilogue<Est::kVtrace, ITEMS, VEC>(pv, c, A, a_after, row, t0);
+    }
+}
+
 // ------------------------------------------------------------------ warp-owned rows
 
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
