@@ -69,18 +69,18 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
                 else "credit_gae_vtrace_kernel (CTA row loop, GAE and V-trace per load)")
     name = _EST_NAME[est]
     if est == "gae_bf16":
-        return (f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)" if T <= 256
-                else f"credit_warp_kernel<{name}> (warp-owned rows, 16 steps/lane)")
+        if T <= 256:
+            return f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)"
+        return (f"credit_warp_pipe_kernel<{name}> (a warp per row, 2 chunks of loads in flight)"
+                if T <= 1024 else f"credit_warp_kernel<{name}> (warp-owned rows, 16 steps/lane)")
     if T > 1024:
         if workspace and N < 2 * sms:
             return f"credit_scan_kernel<{name}, look-back across CTA tiles>"
         return f"credit_scan_kernel<{name}, CTA row loop>"
     if T <= 256:
         return f"credit_warp_kernel<{name}> (warp-owned rows)"
-    if est == "gae" and T % 16 == 0:
-        return f"credit_warp_stream_kernel<{name}> (warp-owned rows, per-warp TMA ring)"
     if est == "gae":
-        return f"credit_warp_kernel<{name}> (warp-owned rows)"
+        return f"credit_warp_pipe_kernel<{name}> (a warp per row, next chunk's loads in flight)"
     return f"credit_scan_kernel<{name}, whole-row CTA tiles>"
 
 

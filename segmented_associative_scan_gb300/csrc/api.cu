@@ -164,13 +164,7 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
     for (int o = 0; o < n_out; ++o) vec32 = vec32 && (!outs[o] || aligned(outs[o], 32));
     const int vec = vec32 ? 2 : (vec16 ? 1 : 0);
 
-    // The warp-streaming kernel moves chunks of rows longer than one warp chunk with
-    // 16-byte bulk copies: every base 16-byte aligned, ld and T multiples of 16.
-    bool streamable = in_elem == 4 && !p.host && vec16 && (p.ld % 16) == 0 && (p.T % 16) == 0 &&
-                      p.T > rlca::kWarpChunk && aligned(p.term, 16) &&
-                      (!p.trunc || aligned(p.trunc, 16));
-
-    const cudaError_t err = launch(p, vec, streamable, static_cast<cudaStream_t>(stream));
+    const cudaError_t err = launch(p, vec, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? RLCA_OK : RLCA_ERR_LAUNCH;
 }
 
@@ -197,12 +191,6 @@ Params base_params(const float *reward, const uint8_t *term, const uint8_t *trun
 }
 
 // bf16 = the per-step data inputs hold bf16 bit patterns (no workspace then).
-// Adapts a bf16 launcher (no streaming kernel) to the launch signature.
-template <typename F>
-auto bf16_launch(F fn)
-{
-    return [fn](const Params &q, int vec, bool, cudaStream_t s) { return fn(q, vec, s); };
-}
 
 int discounted_return(const float *reward, const uint8_t *terminated, const uint8_t *truncated,
                       const float *trunc_value, const float *bootstrap, float gamma, int64_t N,
@@ -218,7 +206,7 @@ int discounted_return(const float *reward, const uint8_t *terminated, const uint
     const float *in[] = {reward};
     float *out[] = {returns};
     if (bf16)
-        return validate_and_launch(p, in, 1, out, 1, ws, bf16_launch(rlca::launch_return_bf16),
+        return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return_bf16,
                                    stream, 2);
     return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return, stream);
 }
@@ -237,7 +225,7 @@ int td_lambda(const float *reward, const float *value, const uint8_t *terminated
     float *out[] = {targets};
     if (bf16)
         return validate_and_launch(p, in, 2, out, 1, ws,
-                                   bf16_launch(rlca::launch_td_lambda_bf16), stream, 2);
+                                   rlca::launch_td_lambda_bf16, stream, 2);
     return validate_and_launch(p, in, 2, out, 1, ws, rlca::launch_td_lambda, stream);
 }
 
@@ -255,7 +243,7 @@ int gae(const float *reward, const float *value, const uint8_t *terminated,
     const float *in[] = {reward, value};
     float *out[] = {advantages, returns};
     if (bf16)
-        return validate_and_launch(p, in, 2, out, 2, ws, bf16_launch(rlca::launch_gae_bf16),
+        return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae_bf16,
                                    stream, 2);
     return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae, stream);
 }
@@ -281,7 +269,7 @@ int vtrace(const float *reward, const float *value, const float *log_rho,
     const float *in[] = {reward, value, log_rho};
     float *out[] = {vs, pg_advantages};
     if (bf16)
-        return validate_and_launch(p, in, 3, out, 2, ws, bf16_launch(rlca::launch_vtrace_bf16),
+        return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace_bf16,
                                    stream, 2);
     return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace, stream);
 }
@@ -302,7 +290,7 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     const float *in[] = {reward, q_taken, expected_q, rho};
     float *out[] = {q_ret};
     if (bf16)
-        return validate_and_launch(p, in, 4, out, 1, ws, bf16_launch(rlca::launch_retrace_bf16),
+        return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace_bf16,
                                    stream, 2);
     return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
 }
@@ -334,7 +322,7 @@ int gae_vtrace(const float *reward, const float *value, const float *log_rho,
     if (check_shape(N, T, ld, &empty) == RLCA_OK && !empty && !advantages) return RLCA_ERR_NULL;
     const float *in[] = {reward, value, log_rho};
     float *out[] = {vs, advantages, returns, pg_advantages};
-    auto launch = [&pg](const Params &q, int vec, bool, cudaStream_t s) {
+    auto launch = [&pg](const Params &q, int vec, cudaStream_t s) {
         Params g = pg;  // the same validated shape and memory kind as the V-trace half
         g.host = q.host;
         return rlca::launch_gae_vtrace(g, q, vec, s);
@@ -369,7 +357,7 @@ int td_lambda_multi(const float *reward, const float *value, const uint8_t *term
         for (int k = 0; k < n_lambdas; ++k)
             if (!outs[k]) return RLCA_ERR_NULL;
     const float *in[] = {reward, value};
-    auto launch = [](const Params &q, int vec, bool, cudaStream_t s) {
+    auto launch = [](const Params &q, int vec, cudaStream_t s) {
         return rlca::launch_td_multi(q, vec, s);
     };
     return validate_and_launch(p, in, 2, outs, n_lambdas, Workspace{nullptr, 0}, launch,
@@ -389,7 +377,7 @@ int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *trunc
     p.out0 = out;
     const float *in[] = {x};
     float *outs[] = {out};
-    auto launch = [bf16](const Params &q, int vec, bool, cudaStream_t s) {
+    auto launch = [bf16](const Params &q, int vec, cudaStream_t s) {
         return bf16 ? rlca::launch_forward_bf16(q, vec, s) : rlca::launch_forward(q, vec, s);
     };
     return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream,

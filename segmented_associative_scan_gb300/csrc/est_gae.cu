@@ -3,9 +3,9 @@
 #include "launch.cuh"
 
 namespace rlca {
-cudaError_t launch_gae(const Params &p, int vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_gae(const Params &p, int vec, cudaStream_t stream)
 {
-    return launch_estimator<Est::kGae>(p, vec, streamable, stream);
+    return launch_estimator<Est::kGae>(p, vec, stream);
 }
 
 cudaError_t launch_gae_bf16(const Params &p, int vec, cudaStream_t stream)

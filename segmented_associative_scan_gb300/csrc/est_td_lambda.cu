@@ -3,9 +3,9 @@
 #include "launch.cuh"
 
 namespace rlca {
-cudaError_t launch_td_lambda(const Params &p, int vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_td_lambda(const Params &p, int vec, cudaStream_t stream)
 {
-    return launch_estimator<Est::kTdLambda>(p, vec, streamable, stream);
+    return launch_estimator<Est::kTdLambda>(p, vec, stream);
 }
 
 cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream)

@@ -153,6 +153,139 @@ __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0,
         c.y_next = next_item<TIn>(c.y[0], in_row<TIn>(p.rho, off), t0 + ITEMS, need, lane);
 }
 
+// The raw 32-bit words of one thread's ITEMS steps of every array an estimator reads,
+// held in registers between their load and their use, so a warp can ask for the next
+// chunk's words before it scans the current one. Full, aligned chunks only (each array's
+// words fill whole 128-bit loads).
+template <Est E, int ITEMS, typename TIn>
+struct RawChunk {
+    using Tr = EstTraits<E>;
+    static constexpr int kWords = ITEMS * (int)sizeof(TIn) / 4;
+    static_assert(kWords % 4 == 0, "a thread's items fill whole 128-bit loads");
+    uint32_t r[kWords];
+    uint32_t v[Tr::kValue ? kWords : 1];
+    uint32_t x[Tr::kAux ? kWords : 1];
+    uint32_t y[Tr::kRho ? kWords : 1];
+    uint32_t term[ITEMS / 4];
+    uint32_t trunc[ITEMS / 4];
+    float v_next, x_next, y_next;  // thread 31 of a warp: the next chunk's first step
+};
+
+// kWords words of one row from column t0 (VEC bit 1: 256-bit loads, else 128-bit).
+template <int kWords, int VEC, typename TIn>
+__device__ __forceinline__ void load_words(const TIn *__restrict__ row, int t0,
+                                           uint32_t (&w)[kWords])
+{
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(row + t0);
+    if constexpr ((VEC & kWideLoads) && kWords % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < kWords / 8; ++k) {
+            float f[8];
+            ld_stream8(reinterpret_cast<const float *>(src) + 8 * k, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[8 * k + i] = __float_as_uint(f[i]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kWords / 4; ++k) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(src) + k);
+            w[4 * k] = q.x;
+            w[4 * k + 1] = q.y;
+            w[4 * k + 2] = q.z;
+            w[4 * k + 3] = q.w;
+        }
+    }
+}
+
+// The flag bytes of ITEMS steps as ITEMS / 4 words (VEC bit 1: 64-bit loads).
+template <int ITEMS, int VEC>
+__device__ __forceinline__ void load_flag_words(const uint8_t *__restrict__ row, int t0,
+                                                uint32_t (&w)[ITEMS / 4])
+{
+    if constexpr ((VEC & kWideLoads) && ITEMS % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 8; ++k) {
+            const uint2 q = ld_stream(reinterpret_cast<const uint2 *>(row + t0) + k);
+            w[2 * k] = q.x;
+            w[2 * k + 1] = q.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k)
+            w[k] = ld_stream(reinterpret_cast<const uint32_t *>(row + t0) + k);
+    }
+}
+
+// Issue the loads of one full chunk of a row (thread's first step t0, t0 + ITEMS <= T).
+// Thread 31 also reads the next chunk's first step, if the row has one.
+template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn>
+__device__ __forceinline__ void load_raw(const Params &p, int64_t off, int t0, int lane,
+                                         RawChunk<E, ITEMS, TIn> &w)
+{
+    using Tr = EstTraits<E>;
+    constexpr int kW = RawChunk<E, ITEMS, TIn>::kWords;
+    load_words<kW, VEC>(in_row<TIn>(p.reward, off), t0, w.r);
+    if constexpr (Tr::kValue) load_words<kW, VEC>(in_row<TIn>(p.value, off), t0, w.v);
+    if constexpr (Tr::kAux) load_words<kW, VEC>(in_row<TIn>(p.aux, off), t0, w.x);
+    if constexpr (Tr::kRho) load_words<kW, VEC>(in_row<TIn>(p.rho, off), t0, w.y);
+    load_flag_words<ITEMS, VEC>(p.term + off, t0, w.term);
+    if constexpr (TRUNC) load_flag_words<ITEMS, VEC>(p.trunc + off, t0, w.trunc);
+    const int tn = t0 + ITEMS;
+    if (lane == 31 && tn < p.T) {
+        if constexpr (Tr::kNextValue) w.v_next = InType<TIn>::cached(in_row<TIn>(p.value, off) + tn);
+        if constexpr (Tr::kNextAux) w.x_next = InType<TIn>::cached(in_row<TIn>(p.aux, off) + tn);
+        if constexpr (Tr::kNextRho) w.y_next = InType<TIn>::cached(in_row<TIn>(p.rho, off) + tn);
+    }
+}
+
+template <typename TIn, int ITEMS, int kWords>
+__device__ __forceinline__ void widen_words(const uint32_t (&w)[kWords], float (&x)[ITEMS])
+{
+    constexpr int PV = InType<TIn>::kPerVec;
+#pragma unroll
+    for (int k = 0; k < ITEMS / PV; ++k)
+        InType<TIn>::unpack(make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]),
+                            x + PV * k);
+}
+
+// A full chunk's Chunk from its raw words (what load_chunk forms from its loads).
+// Every thread of the warp must call this (it shuffles).
+template <Est E, int ITEMS, bool TRUNC, typename TIn>
+__device__ __forceinline__ void unpack_raw(const RawChunk<E, ITEMS, TIn> &w, int T, int t0,
+                                           int lane, Chunk<ITEMS> &c)
+{
+    using Tr = EstTraits<E>;
+    widen_words<TIn>(w.r, c.r);
+    if constexpr (Tr::kValue) widen_words<TIn>(w.v, c.v);
+    if constexpr (Tr::kAux) widen_words<TIn>(w.x, c.x);
+    if constexpr (Tr::kRho) widen_words<TIn>(w.y, c.y);
+    unsigned term = 0, trunc = 0;
+#pragma unroll
+    for (int k = 0; k < ITEMS / 4; ++k) {
+        term |= nonzero_bytes(w.term[k]) << (4 * k);
+        if constexpr (TRUNC) trunc |= nonzero_bytes(w.trunc[k]) << (4 * k);
+    }
+    c.term = term;
+    c.trunc = trunc;
+    c.valid = all_items<ITEMS>();
+    const int last = T - 1 - t0;
+    const unsigned window_end = (last >= 0 && last < ITEMS) ? (1u << last) : 0u;
+    c.stop = (term | trunc | window_end) & all_items<ITEMS>();
+    const bool need = t0 + ITEMS < T;  // false only for the row's last thread
+    if constexpr (Tr::kNextValue) {
+        const float s = __shfl_down_sync(kFullMask, c.v[0], 1);
+        c.v_next = need ? (lane == 31 ? w.v_next : s) : 0.f;
+    }
+    if constexpr (Tr::kNextAux) {
+        const float s = __shfl_down_sync(kFullMask, c.x[0], 1);
+        c.x_next = need ? (lane == 31 ? w.x_next : s) : 0.f;
+    }
+    if constexpr (Tr::kNextRho) {
+        const float s = __shfl_down_sync(kFullMask, c.y[0], 1);
+        c.y_next = need ? (lane == 31 ? w.y_next : s) : 0.f;
+    }
+}
+
 template <int ITEMS>
 __device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next, int j)
 {

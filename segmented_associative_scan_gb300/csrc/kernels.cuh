@@ -29,8 +29,9 @@
 //              inclusive value at once, so look-back never passes an episode boundary.
 //
 // Also here: the fused kernels (TD(lambda) for several lambdas, GAE with V-trace: one
-// load of a tile, one scan per estimator) and the warp-owned-rows kernel (a warp scans
-// whole short rows, or walks a row in warp-sized chunks, with no CTA barrier).
+// load of a tile, one scan per estimator), the warp-owned-rows kernel (a warp scans
+// whole short rows, or walks a row in warp-sized chunks, with no CTA barrier) and its
+// pipelined form (a warp per row that keeps the next chunks' loads in flight).
 #pragma once
 
 #include "estimators.cuh"
@@ -454,13 +455,11 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_gae_vtrace_warp_kerne
 // One warp scans a chunk of 32 * ITEMS steps with no help from other warps: lane
 // aggregates, a warp suffix scan, and the chunk's carry-in (A at the step after the
 // chunk) applied directly. Returns A at the chunk's first step.
-template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
-__device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0, bool active,
-                                            float carry_in)
+template <Est E, int ITEMS, int VEC, typename TIn = float>
+__device__ __forceinline__ float warp_chunk_scan(const Params &p, int64_t row, int t0,
+                                                 Chunk<ITEMS> &c, float carry_in)
 {
     const int lane = threadIdx.x & 31;
-    Chunk<ITEMS> c;
-    load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, t0, active, lane, c);
     Affine e[ITEMS];
     build<E, ITEMS, TIn>(p, row, t0, c, e);
     const Affine agg = thread_aggregate<E, ITEMS>(p, c, e);
@@ -473,6 +472,16 @@ __device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0
     replay<E, ITEMS>(p, c, e, a_after, A);
     epilogue<E, ITEMS, VEC>(p, c, A, a_after, row, t0);
     return affine_apply(whole, carry_in);
+}
+
+// The same, loading the chunk first (ragged and inactive chunks allowed).
+template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
+__device__ __forceinline__ float warp_chunk(const Params &p, int64_t row, int t0, bool active,
+                                            float carry_in)
+{
+    Chunk<ITEMS> c;
+    load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, t0, active, threadIdx.x & 31, c);
+    return warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, carry_in);
 }
 
 // Every warp of the grid owns one job, with no barrier and no shared memory:
@@ -503,6 +512,52 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Par
         for (int s = p.segs - 1; s >= 0; --s)
             carry = warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, job, s * CH + lane * ITEMS, true,
                                                           carry);
+    }
+}
+
+// Warp-owned rows with the next chunks' loads in flight: one row per warp, walked in
+// chunks of 32 * ITEMS steps from the last to the first. Before a chunk is scanned, the
+// warp has already asked for the raw words of the DEPTH chunks before it (registers as a
+// software pipeline), so its HBM reads overlap its own scans and stores instead of
+// alternating with them. A ragged last chunk is scanned on its own through the plain
+// load before the pipeline starts; every chunk after that is full. Needs 16-byte aligned
+// rows (VEC >= 1) and T > 32 * ITEMS. MINB: CTAs per SM the register allocator must fit
+// (0 = no request).
+template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4,
+          typename TIn = float, int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(const Params p)
+{
+    static_assert(DEPTH == 1 || DEPTH == 2, "one or two chunks in flight");
+    static_assert(VEC & kVec16, "raw chunks are read with vector loads");
+    grid_dependency_sync();
+    constexpr int CH = 32 * ITEMS;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= p.N) return;  // the whole warp leaves together
+    const int64_t off = row * p.ld;
+    int s = p.segs - 1;
+    float carry = 0.f;
+    if (p.T != p.segs * CH) {
+        carry = warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, s * CH + lane * ITEMS, true, 0.f);
+        --s;
+    }
+    if (s < 0) return;
+    RawChunk<E, ITEMS, TIn> w0, w1;
+    load_raw<E, ITEMS, VEC, TRUNC>(p, off, s * CH + lane * ITEMS, lane, w0);
+    if (DEPTH == 2 && s >= 1)
+        load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w1);
+    for (; s >= 0; --s) {
+        const int t0 = s * CH + lane * ITEMS;
+        Chunk<ITEMS> c;
+        unpack_raw<E, ITEMS, TRUNC>(w0, p.T, t0, lane, c);
+        if (DEPTH == 2) {
+            w0 = w1;
+            if (s >= 2)
+                load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 2) * CH + lane * ITEMS, lane, w1);
+        } else if (s >= 1) {
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w0);
+        }
+        carry = warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, carry);
     }
 }
 

@@ -11,7 +11,6 @@
 #include <type_traits>
 
 #include "kernels.cuh"
-#include "warp_stream.cuh"
 
 namespace rlca {
 
@@ -58,7 +57,7 @@ cudaError_t launch_pdl(Kernel kernel, unsigned grid, unsigned block, size_t smem
 
 // ------------------------------------------------------------------ kernel choice
 
-enum class Path : int { kCtaRows, kCtaRowLoop, kLookback, kWarpRows, kWarpStream };
+enum class Path : int { kCtaRows, kCtaRowLoop, kLookback, kWarpRows, kWarpPipe };
 
 constexpr int kMaxDevices = 64;
 
@@ -85,20 +84,22 @@ inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 // Measured on GB300 (CUDA-event timing, inputs rotated past L2): rows of at most one
 // warp chunk (256 steps) go to warp-owned rows, which need no CTA barrier; up to one CTA
 // tile (1024 steps) the CTA tile kernel, which loads a whole row at once, wins for every
-// estimator but GAE with truncation: there the dependent load of the truncation values
-// stalls a whole CTA, and the barrier-free warp-streaming kernel is 8% faster (14.7 vs
-// 16.1 us at [4096, 1024]); without truncation the CTA kernel is 6% faster (12.7 vs
-// 13.5 us). Longer rows loop over CTA tiles (or use look-back with a workspace). Data in
-// pinned host memory never take the bulk-copy kernel; GAE then uses CTA tiles (a GAE
-// step at [4096, 1024] over NVLink-C2C: 275 us, at 335 GB/s).
+// estimator but GAE with truncation (or rows of at most 512 steps): there the dependent
+// load of the truncation values stalls a whole CTA, and a warp per row that keeps its
+// next chunk's loads in flight (credit_warp_pipe_kernel) is fastest: at [4096, 1024]
+// 12.90 us against 13.90 for a per-warp TMA ring of bulk copies (itself 8% faster than
+// the CTA tile there); 7.29 vs 8.25 at [4096, 512], 5.38 vs 6.04 at [1024, 1024].
+// Without truncation the CTA tile stays. Longer rows loop over CTA tiles (or use
+// look-back with a workspace). Data in pinned host memory take the CTA tiles for GAE
+// too (a GAE step at [4096, 1024] over NVLink-C2C: 275 us, at 335 GB/s).
+// `aligned`: rows fit for 128-bit access.
 template <Est E>
-inline Path choose_path(int64_t N, int T, bool streamable, bool lookback, bool trunc,
-                        bool host)
+inline Path choose_path(int64_t N, int T, bool aligned, bool lookback, bool trunc, bool host)
 {
     if (T > kTile) return lookback && lookback_pays(N) ? Path::kLookback : Path::kCtaRowLoop;
     if (T <= 32 * kItems) return Path::kWarpRows;
     if (E == Est::kGae && (trunc || 2 * T <= kTile) && !host)
-        return streamable ? Path::kWarpStream : Path::kWarpRows;
+        return aligned ? Path::kWarpPipe : Path::kWarpRows;
     return Path::kCtaRows;
 }
 
@@ -183,47 +184,19 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
                       grid, 32 * kWarpsPerCta, 0, stream, p);
 }
 
-// Per-device grid limit (SMs x resident CTAs) of the warp-streaming kernel.
-template <Est E, bool TRUNC>
-struct WarpStreamConfig {
-    static std::atomic<int> grid_limit[kMaxDevices];
-};
-template <Est E, bool TRUNC>
-std::atomic<int> WarpStreamConfig<E, TRUNC>::grid_limit[kMaxDevices];
-
-template <Est E, bool TRUNC>
-cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
+// One row per warp, kItems steps per lane, DEPTH chunks' loads in flight ahead of the
+// scan (credit_warp_pipe_kernel). Rows longer than one warp chunk, 16-byte aligned.
+template <Est E, int VEC, bool TRUNC, int DEPTH, typename TIn = float, int MINB = 0>
+cudaError_t launch_warp_pipe(Params p, cudaStream_t stream)
 {
-    auto kernel = credit_warp_stream_kernel<E, TRUNC, kWarpsPerCta>;
-    const int smem = kWarpsPerCta * warp_stages<E>() * WarpStage<E>::kBytes;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    int limit = WarpStreamConfig<E, TRUNC>::grid_limit[dev].load(std::memory_order_relaxed);
-    if (limit == 0) {
-        int sms = 0, per_sm = 0;
-        if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem)) != cudaSuccess ||
-            (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) !=
-                cudaSuccess ||
-            (err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel,
-                                                                 32 * kWarpsPerCta, smem)) !=
-                cudaSuccess)
-            return err;
-        limit = sms * (per_sm > 0 ? per_sm : 1);
-        WarpStreamConfig<E, TRUNC>::grid_limit[dev].store(limit, std::memory_order_relaxed);
-    }
-    // Rows longer than one warp chunk (the dispatch sends shorter rows to warp-owned
-    // rows): each warp walks whole rows chunk by chunk.
-    p.segs = (p.T + kWarpChunk - 1) / kWarpChunk;
+    constexpr int CH = 32 * kItems;
+    p.segs = (p.T + CH - 1) / CH;
+    p.chunks_per_row = CH / kItems;
     p.rows_per_tile = 1;
-    const int64_t units = p.N;
-    const int64_t warps = (int64_t)limit * kWarpsPerCta;
-    const int64_t per_warp = (units + warps - 1) / warps;  // equal shares, one apart at most
-    const int64_t used = (units + per_warp - 1) / per_warp;
-    const unsigned grid = (unsigned)((used + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(kernel, grid, 32 * kWarpsPerCta, smem, stream, p);
+    const unsigned grid = (unsigned)((p.N + kWarpsPerCta - 1) / kWarpsPerCta);
+    return launch_pdl(
+        credit_warp_pipe_kernel<E, kItems, VEC, TRUNC, DEPTH, kWarpsPerCta, TIn, MINB>, grid,
+        32 * kWarpsPerCta, 0, stream, p);
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -240,7 +213,8 @@ cudaError_t launch_warp_stream(Params p, cudaStream_t stream)
 //   one row per CTA [4096, 1024]: return 7.71 vs 7.52, GAE 12.52 vs 12.05, V-trace 16.88
 //     vs 16.70, fused TD 17.33 vs 17.11, but TD 10.07 vs 10.16, Retrace 15.22 vs 15.36
 //     and the forward scan 8.46 vs 8.53, which keep 128-bit access there;
-//   the warp-streaming GAE (stores only) 14.48 vs 15.16: it keeps 128-bit stores.
+//   pipelined warp rows, GAE [4096, 1024]: 12.90 with 128-bit access, 13.24 with
+//     256-bit, 13.27 with 256-bit loads and 128-bit stores: 128-bit there.
 // Wide loads alone or wide stores alone were slower than either.
 constexpr int kWideVec = kVec16 | kWideLoads | kWideStores;
 
@@ -279,27 +253,47 @@ void set_beta_pow(Params &p)
     for (int i = 1; i < kItems; ++i) p.beta_pow = beta * p.beta_pow;
 }
 
-// bf16 per-step inputs (uint16_t bit patterns, fp32 arithmetic): warp-owned rows up to
-// one warp chunk, CTA tiles (whole rows or the row loop) beyond; GAE rows longer than a
-// warp chunk go to warp-owned rows with 16 steps per lane (measured fastest for bf16).
+// bf16 per-step inputs (uint16_t bit patterns, fp32 arithmetic). Measured on GB300 at
+// [4096, 1024], us per launch, the tiles below against a warp per row with its next
+// chunks' loads in flight (credit_warp_pipe_kernel): GAE 14.15 vs 10.84, TD(lambda)
+// 10.64 vs 8.38, V-trace 20.95 vs 14.32, Retrace 15.33 vs 10.24, return 7.86 vs 7.69;
+// GAE at [16384, 512] 28.33 vs 20.32. So rows longer than two warp chunks (GAE: one)
+// up to one CTA tile take the pipelined warp rows, with two chunks in flight (one for
+// V-trace and Retrace, whose larger raw chunks then keep one wave of warps resident:
+// 14.32 vs 14.59 and 10.24 vs 12.55) and 64-bit flag loads where rows are 32-byte
+// aligned (256-bit stores: GAE 12.77 vs 10.84). Otherwise warp-owned rows up to one
+// warp chunk, CTA tiles (whole rows or the row loop) beyond; GAE rows longer than a warp
+// chunk go to warp-owned rows with 16 steps per lane there.
 template <Est E>
 cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stream)
 {
     Params p = p_in;
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
+    const int pipe_from = E == Est::kGae ? 32 * kItems : 64 * kItems;
+    if (!p.host && vec >= 1 && p.T > pipe_from && p.T <= kTile) {
+        constexpr int D = (E == Est::kVtrace || E == Est::kRetrace) ? 1 : 2;
+        constexpr int kFlags64 = kVec16 | kWideLoads;
+        if (vec >= 2)
+            return trunc ? launch_warp_pipe<E, kFlags64, true, D, uint16_t>(p, stream)
+                         : launch_warp_pipe<E, kFlags64, false, D, uint16_t>(p, stream);
+        return trunc ? launch_warp_pipe<E, kVec16, true, D, uint16_t>(p, stream)
+                     : launch_warp_pipe<E, kVec16, false, D, uint16_t>(p, stream);
+    }
     // bf16 data loads stay 128-bit; wide flag loads and output stores were measured
     // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout
     // in device memory.
     if (!p.host) vec = vec < 1 ? vec : 1;
-    if (E == Est::kGae && p.T > 32 * kItems) {
-        // 16 steps per lane: beta^16 for the per-lane composite.
-        p.beta_pow = p.gamma_lambda;
-        for (int i = 1; i < 16; ++i) p.beta_pow = p.gamma_lambda * p.beta_pow;
-        return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
-            return launch_warp_rows<E, decltype(v)::value, decltype(r)::value, uint16_t, 16>(
-                p, stream);
-        });
+    if constexpr (E == Est::kGae) {
+        if (p.T > 32 * kItems) {
+            // 16 steps per lane: beta^16 for the per-lane composite.
+            p.beta_pow = p.gamma_lambda;
+            for (int i = 1; i < 16; ++i) p.beta_pow = p.gamma_lambda * p.beta_pow;
+            return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
+                return launch_warp_rows<E, decltype(v)::value, decltype(r)::value, uint16_t,
+                                        16>(p, stream);
+            });
+        }
     }
     const Path path = p.T <= 32 * kItems ? Path::kWarpRows
                                          : (p.T > kTile ? Path::kCtaRowLoop : Path::kCtaRows);
@@ -312,18 +306,19 @@ cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stre
 }
 
 // Launch one estimator; `vec` = access level (0 scalar, 1 16-byte aligned rows with
-// 128-bit access, 2 32-byte aligned rows fit for 256-bit access), `streamable` = layout
-// fit for 16-byte bulk copies (see api.cu).
+// 128-bit access, 2 32-byte aligned rows fit for 256-bit access).
 template <Est E>
-cudaError_t launch_estimator(const Params &p_in, int vec, bool streamable, cudaStream_t stream)
+cudaError_t launch_estimator(const Params &p_in, int vec, cudaStream_t stream)
 {
     Params p = p_in;
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
-    const Path path = choose_path<E>(p.N, p.T, streamable, p.ws != nullptr, trunc, p.host);
-    if (path == Path::kWarpStream)
-        return trunc ? launch_warp_stream<E, true>(p, stream)
-                     : launch_warp_stream<E, false>(p, stream);
+    const Path path = choose_path<E>(p.N, p.T, vec >= 1, p.ws != nullptr, trunc, p.host);
+    if constexpr (E == Est::kGae) {
+        if (path == Path::kWarpPipe)
+            return trunc ? launch_warp_pipe<E, kVec16, true, 1>(p, stream)
+                         : launch_warp_pipe<E, kVec16, false, 1>(p, stream);
+    }
     if ((E == Est::kTdLambda || E == Est::kRetrace) && path == Path::kCtaRows &&
         one_row_per_cta(p.T) && !p.host)
         vec = vec < 1 ? vec : 1;
@@ -333,11 +328,11 @@ cudaError_t launch_estimator(const Params &p_in, int vec, bool streamable, cudaS
 }
 
 // One definition per estimator, each in its own translation unit.
-cudaError_t launch_return(const Params &p, int vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_td_lambda(const Params &p, int vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_gae(const Params &p, int vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_vtrace(const Params &p, int vec, bool streamable, cudaStream_t stream);
-cudaError_t launch_retrace(const Params &p, int vec, bool streamable, cudaStream_t stream);
+cudaError_t launch_return(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_td_lambda(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_gae(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_vtrace(const Params &p, int vec, cudaStream_t stream);
+cudaError_t launch_retrace(const Params &p, int vec, cudaStream_t stream);
 // The same with bf16 per-step inputs.
 cudaError_t launch_return_bf16(const Params &p, int vec, cudaStream_t stream);
 cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream);

@@ -76,12 +76,13 @@ class Placed:
 
 def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0",
             check_guards=True, drop_second_output=False, workspace=None,
-            in_dtype=torch.float32, host=None):
+            in_dtype=torch.float32, host=None, out_offset=None):
     """Run `est` on the CUDA path; returns {output name: float64 array}. `workspace`
     (a zeroed uint8 CUDA tensor) selects the look-back (_ex) entry point; in_dtype
     torch.bfloat16 places the data inputs as bf16 (the _bf16 entry points). `host`
     ("all", "inputs" or "outputs") places those buffers in pinned host memory, which
-    the kernels then read or write in place."""
+    the kernels then read or write in place. `out_offset` places the outputs at another
+    element offset than the inputs."""
     N, T = ro.N, ro.T
     in_dev = "pinned" if host in ("all", "inputs") else device
     out_dev = "pinned" if host in ("all", "outputs") else device
@@ -104,7 +105,8 @@ def run_gpu(est, ro, params, ld=None, offset=0, bool_flags=False, device="cuda:0
         boot = boot.pin_memory() if in_dev == "pinned" else boot.to(device)
     r, term, trunc = f32(ro.reward), flag(ro.terminated), flag(ro.truncated)
     tv = f32(ro.trunc_value) if ro.truncated is not None else None
-    outs = {name: Placed(None, N, T, ld, offset, torch.float32, SENTINEL, out_dev)
+    out_off = offset if out_offset is None else out_offset
+    outs = {name: Placed(None, N, T, ld, out_off, torch.float32, SENTINEL, out_dev)
             for name in OUTPUTS[est]}
     if drop_second_output and len(outs) == 2:
         outs.pop(OUTPUTS[est][1])

@@ -44,8 +44,8 @@ def test_bf16_layouts(ld_extra, offset):
 @pytest.mark.parametrize("ld_extra,offset", [(0, 0), (16, 0), (16, 8)])
 @pytest.mark.parametrize("T", [272, 512, 768, 1024])
 def test_bf16_gae_rows(T, ld_extra, offset, trunc):
-    """bf16 GAE on rows of 257-1024 steps (warp-owned rows, 16 steps per lane), with
-    and without truncation, on padded and offset layouts."""
+    """bf16 GAE on rows of 257-1024 steps (pipelined warp-owned rows), with and without
+    truncation, on padded and offset layouts."""
     ro = bf16_rounded(sr.generic(40, T, seed=T + ld_extra + offset, p_term=0.01,
                                  p_trunc=0.005 if trunc else 0.0))
     if not trunc:

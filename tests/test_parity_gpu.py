@@ -163,7 +163,7 @@ def test_row_stride_and_alignment(ld_extra, offset, T):
 @pytest.mark.parametrize("T", [257, 300, 512, 513, 777, 1023, 1024])
 def test_without_truncation(ld_extra, offset, T):
     """No truncation tensor at all: GAE rows longer than half a tile then take the CTA
-    kernel (one row per CTA) instead of the warp-streaming kernel."""
+    kernel (one row per CTA) instead of the pipelined warp-owned rows."""
     ro = sr.generic(37, T, seed=90 + T, p_term=0.01, p_trunc=0.0)
     ro.truncated = None
     for est in ESTIMATORS:
@@ -176,8 +176,8 @@ def test_without_truncation(ld_extra, offset, T):
 @pytest.mark.parametrize("T", [256, 1024, 2048])
 def test_access_widths(ld_extra, offset, T):
     """Each access width on the same inputs: 256-bit (32-byte aligned rows: ld % 8 == 0,
-    offset 0), 128-bit (offset 4 floats or ld % 8 == 4), scalar (offset 2). For GAE with
-    truncation at T = 1024 the warp-streaming kernel takes both store widths."""
+    offset 0), 128-bit (offset 4 floats or ld % 8 == 4), scalar (offset 2). GAE with
+    truncation at T = 1024 takes the pipelined warp-owned rows at both aligned levels."""
     ro = sr.generic(29, T, seed=70 + T + ld_extra + offset, p_term=0.01, p_trunc=0.005)
     for est in ESTIMATORS:
         g = run_gpu(est, ro, {}, ld=T + ld_extra, offset=offset)
