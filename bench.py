@@ -62,7 +62,12 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
         return ("credit_forward_tile_kernel (whole-row CTA tiles, forward)" if T <= 1024
                 else "credit_forward_tile_kernel (CTA row loop, forward)")
     if est == "td_multi":
-        return ("credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)" if T <= 1024
+        if T <= 256:
+            return "credit_td_multi_warp_kernel (warp-owned rows, 3 lambdas per load)"
+        if T <= 512:
+            return "credit_td_multi_kernel (whole-row CTA tiles, 3 lambdas per load)"
+        return ("credit_td_multi_pipe_kernel (a warp per row, next chunk's loads in flight, "
+                "3 lambdas per load)" if T <= 1024
                 else "credit_td_multi_kernel (CTA row loop, 3 lambdas per load)")
     if est == "gae_vtrace":
         return ("credit_gae_vtrace_kernel (CTA tiles, GAE and V-trace per load)" if T <= 1024

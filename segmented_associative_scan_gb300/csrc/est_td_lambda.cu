@@ -12,7 +12,15 @@ cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream)
 {
     return launch_estimator_bf16<Est::kTdLambda>(p, vec, stream);
 }
-// Fused TD(lambda) for several lambdas: whole-row CTA tiles, or the row loop.
+// Fused TD(lambda) on pipelined warp rows: CTAs per SM the register allocator must fit.
+// Measured on GB300 at [4096, 1024], lambda in {0, 0.9, 1}: 15.58 us capped at 7 per SM,
+// 17.16 uncapped (72 registers either way), 15.93 with 256-bit access, 18.76 with two
+// chunks in flight (95 registers), against 17.30 for one row per CTA.
+constexpr int kMultiPipeMinBlocks = 7;
+
+// Fused TD(lambda) for several lambdas: warp-owned rows up to one warp chunk, pipelined
+// warp rows for rows of 513-1024 steps in device memory with 16-byte aligned rows,
+// whole-row CTA tiles otherwise, and the row loop beyond 1024 steps.
 template <int VEC, bool TRUNC>
 cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
 {
@@ -26,6 +34,17 @@ cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
         const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
         return launch_pdl(credit_td_multi_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
                           32 * kWarpsPerCta, 0, stream, p);
+    }
+    if constexpr ((VEC & kVec16) != 0) {
+        if (2 * p.T > kTile && p.T <= kTile && !p.host) {
+            p.segs = (p.T + CH - 1) / CH;
+            p.chunks_per_row = CH / kItems;
+            p.rows_per_tile = 1;
+            const unsigned grid = (unsigned)((p.N + kWarpsPerCta - 1) / kWarpsPerCta);
+            return launch_pdl(credit_td_multi_pipe_kernel<kItems, kVec16, TRUNC, 1, kWarpsPerCta,
+                                                          kMultiPipeMinBlocks>,
+                              grid, 32 * kWarpsPerCta, 0, stream, p);
+        }
     }
     if (p.T <= kTile) {
         const int t_pad = (p.T + kItems - 1) / kItems * kItems;

@@ -515,30 +515,26 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Par
     }
 }
 
-// Warp-owned rows with the next chunks' loads in flight: one row per warp, walked in
-// chunks of 32 * ITEMS steps from the last to the first. Before a chunk is scanned, the
-// warp has already asked for the raw words of the DEPTH chunks before it (registers as a
-// software pipeline), so its HBM reads overlap its own scans and stores instead of
-// alternating with them. A ragged last chunk is scanned on its own through the plain
-// load before the pipeline starts; every chunk after that is full. Needs 16-byte aligned
-// rows (VEC >= 1) and T > 32 * ITEMS. MINB: CTAs per SM the register allocator must fit
-// (0 = no request).
-template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4,
-          typename TIn = float, int MINB = 0>
-__global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(const Params p)
+// Walks one row per warp in chunks of 32 * ITEMS steps from the last to the first with
+// the next chunks' loads in flight: before a chunk is scanned, the warp has already
+// asked for the raw words of the DEPTH chunks before it (registers as a software
+// pipeline), so its HBM reads overlap its own scans and stores instead of alternating
+// with them. A ragged last chunk goes first through the plain load, before the
+// pipeline starts; every chunk after that is full. scan(t0, c) scans one loaded chunk
+// (thread's first step t0). Needs 16-byte aligned rows (VEC >= 1).
+template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, typename TIn, typename Scan>
+__device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan &&scan)
 {
     static_assert(DEPTH == 1 || DEPTH == 2, "one or two chunks in flight");
     static_assert(VEC & kVec16, "raw chunks are read with vector loads");
-    grid_dependency_sync();
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
-    if (row >= p.N) return;  // the whole warp leaves together
     const int64_t off = row * p.ld;
     int s = p.segs - 1;
-    float carry = 0.f;
     if (p.T != p.segs * CH) {
-        carry = warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, s * CH + lane * ITEMS, true, 0.f);
+        Chunk<ITEMS> c;
+        load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, s * CH + lane * ITEMS, true, lane, c);
+        scan(s * CH + lane * ITEMS, c);
         --s;
     }
     if (s < 0) return;
@@ -557,8 +553,48 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(cons
         } else if (s >= 1) {
             load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w0);
         }
-        carry = warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, carry);
+        scan(t0, c);
     }
+}
+
+// Pipelined warp-owned rows (warp_pipe_row): one row per warp, T > 32 * ITEMS. MINB:
+// CTAs per SM the register allocator must fit (0 = no request).
+template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4,
+          typename TIn = float, int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(const Params p)
+{
+    grid_dependency_sync();
+    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= p.N) return;  // the whole warp leaves together
+    float carry = 0.f;
+    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, TIn>(p, row, [&](int t0, Chunk<ITEMS> &c) {
+        carry = warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, carry);
+    });
+}
+
+// Fused TD(lambda) on pipelined warp-owned rows: each loaded chunk is scanned once per
+// lambda, each lambda with its own carry.
+template <int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4, int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_td_multi_pipe_kernel(const Params p)
+{
+    constexpr Est E = Est::kTdLambda;
+    grid_dependency_sync();
+    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= p.N) return;
+    float carry[kMaxLambdas] = {0.f, 0.f, 0.f, 0.f};
+    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, float>(p, row, [&](int t0, Chunk<ITEMS> &c) {
+#pragma unroll
+        for (int k = 0; k < kMaxLambdas; ++k) {
+            if (k < p.multi.count) {
+                Params q = p;
+                q.gamma_lambda = p.multi.gamma_lambda[k];
+                q.gamma_one_m_lambda = p.multi.gamma_one_m_lambda[k];
+                q.beta_pow = p.multi.beta_pow[k];
+                q.out0 = p.multi.out[k];
+                carry[k] = warp_chunk_scan<E, ITEMS, VEC>(q, row, t0, c, carry[k]);
+            }
+        }
+    });
 }
 
 }  // namespace rlca

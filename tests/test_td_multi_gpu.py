@@ -97,3 +97,33 @@ def test_wide_access_with_ragged_tails(T):
         ref = oracle.td_lambda(ro.reward, ro.value, ro.terminated, ro.truncated,
                                ro.trunc_value, ro.bootstrap, gamma=0.99, lam=lam)
         assert_parity({"t": g}, {"t": ref}, f"td multi lambda={lam} T={T}")
+
+
+@pytest.mark.parametrize("trunc", [True, False])
+@pytest.mark.parametrize("T", [513, 520, 777, 1000, 1016, 1023, 1024])
+def test_pipelined_rows(T, trunc):
+    """Rows of 513-1024 steps take the pipelined warp rows (a warp per row with the next
+    chunk's loads in flight): 3-4 chunks per row, ragged first chunks, with and without
+    truncation, one to four lambdas."""
+    ro = sr.generic(37, T, seed=6000 + T, p_term=0.01, p_trunc=0.01 if trunc else 0.0)
+    if not trunc:
+        ro.truncated = None
+    for lams in ([0.9], [0.0, 0.9, 1.0], [0.0, 0.5, 0.95, 1.0]):
+        got = run(ro, lams)
+        for g, lam in zip(got, lams):
+            ref = oracle.td_lambda(ro.reward, ro.value, ro.terminated, ro.truncated,
+                                   ro.trunc_value, ro.bootstrap, gamma=0.99, lam=lam)
+            assert_parity({"t": g}, {"t": ref}, f"T={T} lambdas={lams} lambda={lam}")
+
+
+@pytest.mark.parametrize("ld_extra,offset", [(4, 0), (0, 4), (8, 0), (3, 0)])
+def test_pipelined_rows_layouts(ld_extra, offset):
+    """128-bit rows (ld % 8 == 4, a 16-byte offset), 32-byte rows, and an odd ld, which
+    leaves the pipeline for the scalar CTA tiles."""
+    ro = sr.generic(9, 1000, seed=6100 + ld_extra + offset, p_term=0.01, p_trunc=0.01)
+    lams = [0.0, 0.9, 1.0]
+    got = run(ro, lams, ld=1000 + ld_extra, offset=offset)
+    for g, lam in zip(got, lams):
+        ref = oracle.td_lambda(ro.reward, ro.value, ro.terminated, ro.truncated,
+                               ro.trunc_value, ro.bootstrap, gamma=0.99, lam=lam)
+        assert_parity({"t": g}, {"t": ref}, f"ld+{ld_extra} off={offset} lambda={lam}")
