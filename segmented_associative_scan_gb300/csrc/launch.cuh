@@ -81,8 +81,9 @@ inline int sm_count()
 // look-back is 1.9x faster, at [512, 16384] 1.1x slower, at [2048, 4096] 1.3x slower).
 inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 
-// Measured on GB300 (CUDA-event timing, inputs rotated past L2): rows of at most one
-// warp chunk (256 steps) go to warp-owned rows, which need no CTA barrier; up to one CTA
+// fp32 inputs (bf16: launch_estimator_bf16 below). Measured on GB300 (CUDA-event timing,
+// inputs rotated past L2): rows of at most one warp chunk (256 steps) go to warp-owned
+// rows, which need no CTA barrier; up to one CTA
 // tile (1024 steps) the CTA tile kernel, which loads a whole row at once, wins for every
 // estimator but GAE with truncation (or rows of at most 512 steps): there the dependent
 // load of the truncation values stalls a whole CTA, and a warp per row that keeps its
