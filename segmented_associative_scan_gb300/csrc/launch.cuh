@@ -83,14 +83,14 @@ inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 
 // fp32 inputs (bf16: launch_estimator_bf16 below). Measured on GB300 (CUDA-event timing,
 // inputs rotated past L2): rows of at most one warp chunk (256 steps) go to warp-owned
-// rows, which need no CTA barrier; up to one CTA
-// tile (1024 steps) the CTA tile kernel, which loads a whole row at once, wins for every
-// estimator but GAE with truncation (or rows of at most 512 steps): there the dependent
-// load of the truncation values stalls a whole CTA, and a warp per row that keeps its
-// next chunk's loads in flight (credit_warp_pipe_kernel) is fastest: at [4096, 1024]
-// 12.90 us against 13.90 for a per-warp TMA ring of bulk copies (itself 8% faster than
-// the CTA tile there); 7.29 vs 8.25 at [4096, 512], 5.38 vs 6.04 at [1024, 1024].
-// Without truncation the CTA tile stays. Longer rows loop over CTA tiles (or use
+// rows, which need no CTA barrier; up to one CTA tile (1024 steps) the CTA tile kernel,
+// which loads a whole row at once, wins for every estimator but GAE with truncation (or
+// rows of at most 512 steps): there the dependent load of the truncation values stalls a
+// whole CTA, and a warp per row that keeps its next chunk's loads in flight
+// (credit_warp_pipe_kernel) is fastest: at [4096, 1024] 12.90 us against 13.90 for a
+// per-warp TMA ring of bulk copies (itself 8% faster than the CTA tile there); 7.29 vs
+// 8.25 at [4096, 512], 5.38 vs 6.04 at [1024, 1024]. Without truncation the CTA tile
+// stays. Longer rows loop over CTA tiles (or use
 // look-back with a workspace). Data in pinned host memory take the CTA tiles for GAE
 // too (a GAE step at [4096, 1024] over NVLink-C2C: 275 us, at 335 GB/s).
 // `aligned`: rows fit for 128-bit access.
