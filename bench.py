@@ -50,18 +50,47 @@ WORKLOADS = {
     "trace": "eligibility trace (forward scan), fp32, num_envs=4096, seq_len=1024",
     "prefix_sum": "episodic prefix sum (forward scan), fp32, num_envs=4096, seq_len=1024",
 }
-_EST_NAME = {"gae": "GAE", "gae_bf16": "GAE, bf16 inputs", "return": "return",
-             "td_lambda": "TD(lambda)", "vtrace": "V-trace", "retrace": "Retrace"}
+for _e in ("return", "td_lambda", "vtrace", "retrace", "trace", "prefix_sum"):
+    WORKLOADS[_e + "_bf16"] = WORKLOADS[_e].replace(", fp32,", ", bf16 inputs / fp32 math and "
+                                                    "outputs,")
+for _e in ("gae", "return", "td_lambda", "vtrace", "retrace", "trace", "prefix_sum"):
+    WORKLOADS[_e + "_fp16"] = WORKLOADS[_e].replace(", fp32,", ", fp16 inputs / fp32 math and "
+                                                    "outputs,")
+_EST_NAME = {"gae": "GAE", "return": "return", "td_lambda": "TD(lambda)", "vtrace": "V-trace",
+             "retrace": "Retrace"}
+
+# Estimators with a 16-bit-input variant: "<base>_bf16" / "<base>_fp16" runs the base
+# estimator's _bf16 / _fp16 entry point on the same workload, its per-step data inputs
+# rounded to that format.
+NARROW = {"_bf16": "bfloat16", "_fp16": "float16"}
+
+
+def base_est(est: str) -> str:
+    """The estimator an entry of the bench computes, without its input-format suffix."""
+    for suffix in NARROW:
+        if est.endswith(suffix):
+            return est[:-len(suffix)]
+    return est
+
+
+def data_dtype_of(torch, est: str):
+    """Torch dtype of the per-step data inputs for `est` (None = fp32)."""
+    for suffix, name in NARROW.items():
+        if est.endswith(suffix):
+            return getattr(torch, name)
+    return None
 
 
 def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
     """The kernel the library's dispatch picks for this call (contiguous rows)."""
-    if est in ("trace", "prefix_sum"):
+    be = base_est(est)
+    narrow = be != est
+    if be in ("trace", "prefix_sum"):
         if T <= 256:
             return "credit_forward_kernel (warp-owned rows, forward)"
         return ("credit_forward_tile_kernel (whole-row CTA tiles, forward)" if T <= 1024
                 else "credit_forward_tile_kernel (CTA row loop, forward)")
-    if est == "td_multi":
+    if be == "td_multi":
         if T <= 256:
             return "credit_td_multi_warp_kernel (warp-owned rows, 3 lambdas per load)"
         if T <= 512:
@@ -69,22 +98,29 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
         return ("credit_td_multi_pipe_kernel (a warp per row, next chunk's loads in flight, "
                 "3 lambdas per load)" if T <= 1024
                 else "credit_td_multi_kernel (CTA row loop, 3 lambdas per load)")
-    if est == "gae_vtrace":
+    if be == "gae_vtrace":
         return ("credit_gae_vtrace_kernel (CTA tiles, GAE and V-trace per load)" if T <= 1024
                 else "credit_gae_vtrace_kernel (CTA row loop, GAE and V-trace per load)")
-    name = _EST_NAME[est]
-    if est == "gae_bf16":
+    name = _EST_NAME[be] + (f", {est[len(be) + 1:]} inputs" if narrow else "")
+    if narrow:
         if T <= 256:
             return f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)"
-        return (f"credit_warp_pipe_kernel<{name}> (a warp per row, 2 chunks of loads in flight)"
-                if T <= 1024 else f"credit_warp_kernel<{name}> (warp-owned rows, 16 steps/lane)")
+        pipe_from = 256 if be == "gae" else 512
+        depth = 1 if be in ("vtrace", "retrace") else 2
+        if pipe_from < T <= 1024:
+            return (f"credit_warp_pipe_kernel<{name}> (a warp per row, {depth} chunk(s) of "
+                    "loads in flight)")
+        if be == "gae":
+            return f"credit_warp_kernel<{name}> (warp-owned rows, 16 steps/lane)"
+        return (f"credit_scan_kernel<{name}, whole-row CTA tiles>" if T <= 1024
+                else f"credit_scan_kernel<{name}, CTA row loop>")
     if T > 1024:
         if workspace and N < 2 * sms:
             return f"credit_scan_kernel<{name}, look-back across CTA tiles>"
         return f"credit_scan_kernel<{name}, CTA row loop>"
     if T <= 256:
         return f"credit_warp_kernel<{name}> (warp-owned rows)"
-    if est == "gae":
+    if be == "gae":
         return f"credit_warp_pipe_kernel<{name}> (a warp per row, next chunk's loads in flight)"
     return f"credit_scan_kernel<{name}, whole-row CTA tiles>"
 
@@ -95,7 +131,7 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) per launch measured by ncu (one captured launch, --set full),
 # keyed by (hash of the kernel sources at the time of the capture, estimator, N, T,
 # workspace); null once the kernels change. Within one captured launch the outputs stay
-# in L2, so these are mostly reads. Summaries with the commands: profiles/*_kernel.md.
+# in L2, so these are mostly reads. The committed ncu summaries give the commands.
 _H = "c086cd4238ad4791"
 NCU_TRAFFIC = {
     (_H, "gae", 4096, 1024, False): 44_066_816,
@@ -115,14 +151,16 @@ NCU_TRAFFIC = {
 
 def kernel_source_hash() -> str:
     """Hash of the code that decides which kernel runs and what it does: the device code
-    and launch logic (csrc/*.cuh, csrc/est_*.cu), with comments and blank lines removed
-    so that editing a comment keeps the recorded traffic. The C-ABI validation (api.cu,
-    noalloc.cu) launches nothing itself and is left out."""
+    and launch logic (csrc/*.cuh and the kernel units, csrc/*.cu but the C-ABI files),
+    with comments and blank lines removed so that editing a comment keeps the recorded
+    traffic. The C-ABI validation (api.cu, noalloc.cu) and the measurement copy
+    (measure.cu) launch no estimator kernel themselves and are left out."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_associative_scan_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith(".cuh") or (name.startswith("est_") and name.endswith(".cu")):
+        if name.endswith(".cuh") or (name.endswith(".cu") and
+                                     name not in ("api.cu", "noalloc.cu", "measure.cu")):
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 text = f.read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -142,20 +180,24 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
+# Per-step data input arrays and output arrays of each estimator entry.
+N_DATA_INPUTS = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
+                 "prefix_sum": 1, "td_multi": 2, "gae_vtrace": 3}
+N_OUTPUTS = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
+             "prefix_sum": 1, "td_multi": 3, "gae_vtrace": 4}
+
+
 def algorithmic_bytes(est: str, ro) -> int:
     """Minimal HBM bytes of one launch: every input element the estimator needs read once
     (truncation values only where a step is truncated and not terminated; per-env
     bootstrap values once) and every output written once."""
     n = ro.N * ro.T
-    f32_in = {"return": 1, "td_lambda": 2, "gae": 2, "vtrace": 3, "retrace": 4, "trace": 1,
-              "prefix_sum": 1, "td_multi": 2, "gae_bf16": 2, "gae_vtrace": 3}[est]
-    outs = {"return": 1, "td_lambda": 1, "gae": 2, "vtrace": 2, "retrace": 1, "trace": 1,
-            "prefix_sum": 1, "td_multi": 3, "gae_bf16": 2, "gae_vtrace": 4}[est]
-    in_bytes = 2 if est.endswith("_bf16") else 4
-    b = n * (in_bytes * f32_in + 1 + 4 * outs)
+    be = base_est(est)
+    in_bytes = 4 if be == est else 2
+    b = n * (in_bytes * N_DATA_INPUTS[be] + 1 + 4 * N_OUTPUTS[be])
     if ro.truncated is not None:
         b += n
-        if est not in ("trace", "prefix_sum"):  # forward scans read no truncation values
+        if be not in ("trace", "prefix_sum"):  # forward scans read no truncation values
             b += in_bytes * int(np.count_nonzero(ro.truncated & (1 - ro.terminated)))
     if ro.bootstrap is not None:
         b += 4 * ro.N
@@ -164,7 +206,8 @@ def algorithmic_bytes(est: str, ro) -> int:
 
 def workload_inputs(est: str, N: int, T: int, seed: int):
     """The seeded workload each estimator is quoted on, at [N, T]."""
-    if est in ("gae", "gae_bf16"):
+    est = base_est(est)
+    if est == "gae":
         return sr.gae_trunc(N=N, T=T, seed=seed)
     if est in ("trace", "prefix_sum"):
         return sr.traces(N=N, T=T, seed=seed)
@@ -295,11 +338,12 @@ class DeviceSet:
 
 
 def launch(rlca, est, s, params):
+    est = base_est(est)  # the binding picks the _bf16 entry point from the tensors' dtype
     fl = dict(terminated=s.terminated, truncated=s.truncated,
               trunc_value=s.trunc_value if s.truncated is not None else None)
     g = params["gamma"]
     ws = s.ws
-    if est in ("gae", "gae_bf16"):
+    if est == "gae":
         rlca.rlca_gae(s.reward, s.value, **fl, bootstrap=s.bootstrap, gamma=g,
                       lam=params["lam"], advantages=s.out0, returns=s.out1, workspace=ws)
     elif est == "return":
@@ -336,24 +380,30 @@ def launch(rlca, est, s, params):
 
 def est_params(est, ro):
     p = dict(ro.params)
-    if est == "td_lambda":
+    if base_est(est) == "td_lambda":
         p["lam"] = 0.9
     return p
 
 
-def capture(torch, rlca, est, sets, params, n_steps, first=0):
-    """A CUDA graph of n_steps launches, step i on input set (first + i) % len(sets)."""
+def capture(torch, step, n_sets, n_steps, first=0):
+    """A CUDA graph of n_steps calls step(i), i = (first + k) % n_sets."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for i in range(n_steps):
-            launch(rlca, est, sets[(first + i) % len(sets)], params)
+        for k in range(n_steps):
+            step((first + k) % n_sets)
     return g
 
 
-def timed_replay(torch, graphs):
-    """Replay graphs between two CUDA events on the current stream; ms elapsed."""
+def timed_replay(torch, graphs, lead):
+    """Replay graphs between two CUDA events on the current stream; ms elapsed.
+
+    `lead`, an untimed graph, is replayed first: while the GPU runs it, the host submits
+    the start event and the timed graphs, so the timed region starts with work already
+    queued and holds exactly the launches of `graphs` (their submission latency stays
+    outside the events)."""
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    lead.replay()
     e0.record()
     for g in graphs:
         g.replay()
@@ -368,22 +418,51 @@ def n_sets_for(bytes_per_set):
     return min(64, max(3, int(np.ceil(2.5 * L2_BYTES / bytes_per_set))))
 
 
-def time_workload(torch, rlca, device, peak, est, ro):
+def us_per_step(torch, step, n_sets, launches=300):
+    """Average µs of step(i) over about `launches` back-to-back calls cycling the sets,
+    replayed from a CUDA graph after a warm-up."""
+    for i in range(3):
+        step(i % n_sets)
+    G = 10 * n_sets
+    g = capture(torch, step, n_sets, G)
+    g.replay()
+    reps = max(1, launches // G)
+    ms = timed_replay(torch, [g] * reps, g)
+    return 1000.0 * ms / (G * reps)
+
+
+def copy_pattern(est, s):
+    """The arrays of set `s` that a plain copy with `est`'s byte pattern streams: the
+    estimator's fp32 data inputs, its flag arrays and its outputs."""
+    be = base_est(est)
+    ins = {"return": [s.reward], "td_lambda": [s.reward, s.value], "gae": [s.reward, s.value],
+           "td_multi": [s.reward, s.value], "vtrace": [s.reward, s.value, s.log_rho],
+           "gae_vtrace": [s.reward, s.value, s.log_rho],
+           "retrace": [s.reward, s.q_taken, s.expected_q, s.rho],
+           "trace": [s.value], "prefix_sum": [s.value]}[be]
+    flags = [s.terminated] + ([s.truncated] if s.truncated is not None else [])
+    outs = [s.out0, s.out1, s.out2, s.out3][:N_OUTPUTS[be]]
+    return ins, flags, outs
+
+
+def warp_walk_chunks(est, T):
+    """256-step chunks a warp walks in the kernel the dispatch picks for `est` at T (the
+    pipelined warp rows), else 1 (warp-owned rows, CTA tiles)."""
+    be = base_est(est)
+    walks = (be == "gae" and 256 < T <= 1024) or (be == "td_multi" and 512 < T <= 1024)
+    return -(-T // 256) if walks and be == est else 1
+
+
+def time_workload(torch, rlca, device, peak, est, ro, ceiling=True):
     """One estimator alone on the batch `ro` (copies of it rotating past L2 when it is
-    large enough): µs per launch, achieved GB/s and the roofline fractions."""
+    large enough): µs per launch, achieved GB/s and the roofline fractions; with
+    `ceiling`, also a plain copy of the same bytes in the same launch shape (fp32 inputs)."""
     params = est_params(est, ro)
     nbytes = algorithmic_bytes(est, ro)
-    base = DeviceSet(ro, device, torch.bfloat16 if est.endswith("_bf16") else None)
+    base = DeviceSet(ro, device, data_dtype_of(torch, est))
     n_sets = n_sets_for(nbytes)
     sets = [base] + [base.clone() for _ in range(n_sets - 1)]
-    for i in range(3):
-        launch(rlca, est, sets[i % len(sets)], params)
-    G = 10 * len(sets)
-    g = capture(torch, rlca, est, sets, params, G)
-    g.replay()
-    reps = max(1, 300 // G)
-    ms = timed_replay(torch, [g] * reps)
-    us = 1000.0 * ms / (G * reps)
+    us = us_per_step(torch, lambda i: launch(rlca, est, sets[i], params), n_sets)
     gbs = nbytes / (us * 1e-6) / 1e9
     out = {"us_per_launch": round(us, 3), "algorithmic_bytes": nbytes,
            "bytes_per_step": round(nbytes / (ro.N * ro.T), 3),
@@ -391,17 +470,28 @@ def time_workload(torch, rlca, device, peak, est, ro):
            "frac_of_8tbs": round(gbs / 8000.0, 4),
            "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1),
            "inputs_exceed_l2": n_sets * nbytes > L2_BYTES}
-    del sets, base, g
+    if ceiling and base_est(est) == est:
+        chunks = warp_walk_chunks(est, ro.T)
+        pats = [copy_pattern(est, x) for x in sets]
+        cu = us_per_step(torch, lambda i: rlca.measure_copy(*pats[i], chunks=chunks), n_sets)
+        out["ceiling_us"] = round(cu, 3)
+        out["frac_of_ceiling"] = round(cu / us, 4)
+    del sets, base
     torch.cuda.empty_cache()
     return out
+
+
+ESTIMATORS_1024 = ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi", "gae_vtrace",
+                   "trace", "prefix_sum") + tuple(
+    e + sfx for sfx in NARROW
+    for e in ("return", "td_lambda", "gae", "vtrace", "retrace", "trace", "prefix_sum"))
 
 
 def per_estimator_roofline(torch, rlca, device, peak):
     """Each estimator alone at [4096, 1024] on its own workload's distributions."""
     return {est: time_workload(torch, rlca, device, peak, est,
                                workload_inputs(est, N_ENVS, SEQ_LEN, seed=100))
-            for est in ("return", "td_lambda", "gae", "vtrace", "retrace", "td_multi",
-                        "gae_vtrace", "trace", "prefix_sum", "gae_bf16")}
+            for est in ESTIMATORS_1024}
 
 
 # The workload configurations, each at its own shape and distributions.
@@ -659,7 +749,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     ro0 = workload_inputs(est, N, T, seed=1000 * rank)
     nbytes = algorithmic_bytes(est, ro0)
     n_sets = n_sets_for(nbytes)
-    data_dtype = torch.bfloat16 if est.endswith("_bf16") else None
+    data_dtype = data_dtype_of(torch, est)
     sets = [DeviceSet(ro0, device, data_dtype)]
     for i in range(1, n_sets):
         sets.append(DeviceSet(workload_inputs(est, N, T, 1000 * rank + i), device, data_dtype))
@@ -669,15 +759,19 @@ def gpu_arm(args, rank, world, local_rank, dist):
     params = est_params(est, ro0)
     step_bytes = [algorithmic_bytes(est, s.ro) for s in sets]
 
+    def step(i):
+        launch(rlca, est, sets[i], params)
+
     K, W = args.steps, args.warmup
     for i in range(W):
-        launch(rlca, est, sets[i % n_sets], params)
+        step(i % n_sets)
     torch.cuda.synchronize()
     G = n_sets * max(1, 96 // n_sets)
-    graphs = [capture(torch, rlca, est, sets, params, G)] * (K // G)
+    graphs = [capture(torch, step, n_sets, G)] * (K // G)
     if K % G:
-        graphs.append(capture(torch, rlca, est, sets, params, K % G))
-    graphs[0].replay()
+        graphs.append(capture(torch, step, n_sets, K % G))
+    lead = graphs[0]  # untimed, keeps the GPU busy while the timed graphs are submitted
+    lead.replay()
     torch.cuda.synchronize()
     kernel_bytes_per_step = sum(step_bytes[i % n_sets] for i in range(K)) / K
 
@@ -687,12 +781,12 @@ def gpu_arm(args, rank, world, local_rank, dist):
     # Hold the GPU busy for ~0.5 s before timing so the clock samples see it under load.
     soak_end = time.time() + (0.0 if args.profile else 0.5)
     while time.time() < soak_end:
-        graphs[0].replay()
+        lead.replay()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    ms = timed_replay(torch, graphs)
+    ms = timed_replay(torch, graphs, lead)
     t1 = time.time()
     if dist is not None:
         dist.barrier()
@@ -709,6 +803,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     value = job_throughput(world, N, T, K, ms_max)
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((src_hash, est, N, T, bool(args.workspace)))
+    in_name = est[len(base_est(est)) + 1:] if base_est(est) != est else "fp32"
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 6),
@@ -716,8 +811,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "data": "synthetic: seeded rollouts with the workload's distributions (no dataset)",
         "config": {
             "workload": WORKLOADS[est] if (N, T) == (N_ENVS, SEQ_LEN)
-            else f"{est}, fp32, num_envs={N}, seq_len={T}", "estimator": est, "num_envs": N,
-            "seq_len": T, "gamma": params["gamma"], "lambda": params.get("lam"),
+            else f"{est}, {in_name}, num_envs={N}, seq_len={T}", "estimator": est,
+            "num_envs": N, "seq_len": T, "gamma": params["gamma"], "lambda": params.get("lam"),
             "input_sets": n_sets,
             "entry": "_ex entry point with a caller workspace" if args.workspace
                      else "plain entry point",
@@ -725,12 +820,16 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    f"{nbytes / 1e6:.1f} MB rotate ({n_sets * nbytes / 1e6:.0f} MB > "
                    f"{L2_BYTES / 1e6:.0f} MB L2)") if n_sets * nbytes > L2_BYTES else
                   (f"{n_sets} batches of {nbytes / 1e6:.2f} MB rotate; they fit in L2"),
-            "timing": f"CUDA graphs of {G} launches replayed between CUDA events on the "
-                      "launch stream; one fused kernel launch per step",
+            "timing": f"CUDA graphs of {min(G, K)} launches replayed between CUDA events on "
+                      "the launch stream, after an untimed graph that keeps the GPU busy "
+                      "while they are submitted; one fused kernel launch per step",
             "parallelism": f"replicas{world}: each GPU its own batch, no collective"},
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
+            "traffic_kind": "ncu, one launch: dram__bytes_read.sum + 32 x "
+                            "lts__t_sectors_op_write.sum (bytes written into L2: the outputs "
+                            "stay in L2 until after a captured launch ends)",
             "kernel": kernel_desc(est, N, T, args.workspace,
                                   torch.cuda.get_device_properties(device).multi_processor_count),
             "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),
@@ -741,14 +840,30 @@ def gpu_arm(args, rank, world, local_rank, dist):
     }
     if not args.no_e2e and est == "gae":
         result["e2e"] = e2e_run(torch, rlca, ro0, device, min(K, args.e2e_steps))
-    del graphs, sets
+    del graphs, sets, lead
     torch.cuda.empty_cache()
-    if world == 1 and not args.no_estimators and (N, T) == (N_ENVS, SEQ_LEN):
-        result["estimators"] = per_estimator_roofline(torch, rlca, device, peak)
-        result["configs"] = per_config(torch, rlca, device, peak,
-                                       min(1.0, args.cpu_seconds / 10.0))
     if world == 1 and args.cpu_seconds > 0 and est == "gae":
         result["cpu_baseline"] = cpu_baseline(ro0, args.cpu_seconds)
+    if world == 1 and not args.no_estimators and (N, T) == (N_ENVS, SEQ_LEN):
+        configs = per_config(torch, rlca, device, peak, min(1.0, args.cpu_seconds / 10.0))
+        estimators = per_estimator_roofline(torch, rlca, device, peak)
+        steady = configs.get(f"{est}_trunc_{N}x{T}") if est == "gae" else None
+        if steady is not None:
+            # The same kernel timed over ~300 back-to-back launches on other batches.
+            result["roofline"]["launch_us_steady"] = steady["us_per_launch"]
+            result["roofline"]["frac_steady"] = steady["frac"]
+        if args.detail:
+            with open(args.detail, "w") as f:
+                json.dump({"configs": configs, "estimators": estimators}, f, indent=1)
+        keep = ("us_per_launch", "frac", "ceiling_us", "frac_of_ceiling", "inputs_exceed_l2",
+                "oracle_timesteps_per_s")
+        result["configs"] = {k: {f: v[f] for f in keep if f in v} for k, v in configs.items()}
+        # Last key: each estimator alone at [4096, 1024], us per launch, fraction of the
+        # measured peak and of its plain-copy ceiling.
+        result["estimators"] = {
+            k: [v["us_per_launch"], v["frac"]] + ([v["frac_of_ceiling"]]
+                                                 if "frac_of_ceiling" in v else [])
+            for k, v in estimators.items()}
     return result
 
 
@@ -813,6 +928,9 @@ def main():
     ap.add_argument("--workspace", action="store_true",
                     help="give every call a look-back workspace (the _ex entry points of the "
                          "five reverse estimators)")
+    ap.add_argument("--detail", default=None,
+                    help="also write the full per-configuration and per-estimator tables "
+                         "to this JSON file")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-estimators", action="store_true")
     ap.add_argument("--profile", action="store_true",

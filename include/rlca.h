@@ -145,6 +145,12 @@ int rlca_vtrace(const float *reward, const float *value, const float *log_rho,
  * (window end; nullable = 0).
  * Scan form: A_t = Q^ret_t - Q_t, alpha_t = r_t + gamma E_pi Q(s_{t+1},.) - Q_t,
  * beta_t = gamma c_{t+1}. Output: q_ret [N,ld].
+ * Domain: rho is a ratio of probabilities, rho >= +0. rho_{t+1} = +0 gives c_{t+1} = 0,
+ * exactly as the formula (a NaN or Inf in Q^ret_{t+1} - Q(s_{t+1},a_{t+1}) still turns
+ * Q^ret_t into NaN, since 0 * NaN and 0 * Inf are NaN). A negative ratio, and -0.0, lie
+ * outside the domain and are read as the end of the trace: Q^ret_t then takes nothing
+ * from step t+1 on, not even a NaN or Inf (the scan carries its reset in the sign bit
+ * of beta_t). With finite values that equals the formula with the ratio replaced by +0.
  */
 int rlca_retrace(const float *reward, const float *q_taken, const float *expected_q,
                  const float *rho, const uint8_t *terminated, const uint8_t *truncated,
@@ -207,13 +213,15 @@ int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
                              int64_t ld, float *sums, void *stream);
 
 /*
- * bf16 inputs. The same estimators with every per-step data input (rewards, values,
- * log-ratios, ratios, Q-values, truncation values, x) given as bf16: uint16_t holding the
- * bf16 bit pattern (a torch.bfloat16 tensor qualifies). Each value widens to fp32
- * exactly and all arithmetic is fp32, so the results equal the fp32 entry points' on
- * the widened inputs up to rounding order. Per-env bootstrap / init values and all
- * outputs stay fp32. Rows take 128-bit loads when ld % 8 == 0 and every input base is
- * 16-byte aligned. Arguments, layouts and errors otherwise as the fp32 entry points.
+ * 16-bit inputs: bf16 (the _bf16 entry points) and fp16 (the _fp16 entry points). The
+ * same estimators with every per-step data input (rewards, values, log-ratios, ratios,
+ * Q-values, truncation values, x) given as 16-bit floats: uint16_t holding the bit
+ * pattern (a torch.bfloat16 or torch.float16 tensor qualifies). Each value widens to fp32
+ * exactly (fp16 subnormals and infinities included; NaN stays NaN) and all arithmetic is
+ * fp32, so the results equal the fp32 entry points' on the widened inputs up to rounding
+ * order. Per-env bootstrap / init values and all outputs stay fp32. Rows take 128-bit
+ * loads when ld % 8 == 0 and every input base is 16-byte aligned. Arguments, layouts
+ * and errors otherwise as the fp32 entry points.
  * This halves the bytes of each data input; the pages note that data formats other
  * than the standard one need more work (technical summary, lay text on limitations).
  */
@@ -245,6 +253,37 @@ int rlca_eligibility_trace_bf16(const uint16_t *x, const uint8_t *terminated,
                                 const uint8_t *truncated, const float *init, float decay,
                                 int64_t N, int64_t T, int64_t ld, float *traces, void *stream);
 int rlca_episodic_prefix_sum_bf16(const uint16_t *x, const uint8_t *terminated,
+                                  const uint8_t *truncated, const float *init, int64_t N,
+                                  int64_t T, int64_t ld, float *sums, void *stream);
+
+int rlca_discounted_return_fp16(const uint16_t *reward, const uint8_t *terminated,
+                                const uint8_t *truncated, const uint16_t *trunc_value,
+                                const float *bootstrap, float gamma, int64_t N, int64_t T,
+                                int64_t ld, float *returns, void *stream);
+int rlca_td_lambda_fp16(const uint16_t *reward, const uint16_t *value,
+                        const uint8_t *terminated, const uint8_t *truncated,
+                        const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                        float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
+                        void *stream);
+int rlca_gae_fp16(const uint16_t *reward, const uint16_t *value, const uint8_t *terminated,
+                  const uint8_t *truncated, const uint16_t *trunc_value, const float *bootstrap,
+                  float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
+                  float *advantages, float *returns, void *stream);
+int rlca_vtrace_fp16(const uint16_t *reward, const uint16_t *value, const uint16_t *log_rho,
+                     const uint8_t *terminated, const uint8_t *truncated,
+                     const uint16_t *trunc_value, const float *bootstrap, float gamma,
+                     float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
+                     int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream);
+int rlca_retrace_fp16(const uint16_t *reward, const uint16_t *q_taken,
+                      const uint16_t *expected_q, const uint16_t *rho,
+                      const uint8_t *terminated, const uint8_t *truncated,
+                      const uint16_t *trunc_value, const float *bootstrap_ev, float gamma,
+                      float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
+                      void *stream);
+int rlca_eligibility_trace_fp16(const uint16_t *x, const uint8_t *terminated,
+                                const uint8_t *truncated, const float *init, float decay,
+                                int64_t N, int64_t T, int64_t ld, float *traces, void *stream);
+int rlca_episodic_prefix_sum_fp16(const uint16_t *x, const uint8_t *terminated,
                                   const uint8_t *truncated, const float *init, int64_t N,
                                   int64_t T, int64_t ld, float *sums, void *stream);
 
@@ -333,18 +372,29 @@ int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, 
  * cudaMalloc could fail or stall the device. The paper has no counterpart to this
  * entry point.
  *
- * Same arguments, results and errors as rlca_gae. When T > 1024 it runs the look-back
- * path of rlca_gae_ex on a workspace the library keeps in a static device array of
+ * Same arguments and results as rlca_gae. Calls that rlca_gae would run without a
+ * workspace anyway go to it unchanged, with its error codes: T <= 1024, N at least twice
+ * the SM count (304 on GB300: the rows fill the GPU one CTA per row), and malformed
+ * shapes. Other calls (T > 1024 and fewer rows) run the look-back path of rlca_gae_ex
+ * on a workspace the library keeps in a static device array of
  * 256 + 32 * RLCA_NOALLOC_MAX_TILES bytes (about 1 MiB), which every GPU that loads the
- * library holds until the process exits. Limit: N * ceil(T / 1024) <= RLCA_NOALLOC_MAX_TILES,
- * else RLCA_ERR_WORKSPACE and nothing is enqueued. It calls no allocator.
- *   - The first call on each device sets the array up (looks up its device address with
- *     that device current and zeroes it, synchronously). Make that first call before
- *     any stream capture.
+ * library holds until the process exits. They get rlca_gae_ex's checks, in its order;
+ * a look-back call of more than RLCA_NOALLOC_MAX_TILES tiles (N * ceil(T / 1024)) fails
+ * with RLCA_ERR_WORKSPACE. A call that fails a check enqueues nothing. It calls no
+ * allocator.
+ *   - Set-up: a look-back call looks up the array's device address with the current
+ *     device (cheap; host code cannot use the symbol itself). When the address is new
+ *     to the library (the first such call on a device, or after cudaDeviceReset moved
+ *     the array) it zeroes the whole array first, synchronously. Make the first call on
+ *     each device before any stream capture.
  *   - Every call on a device shares the one array, and the array keeps the previous
- *     call's contents (each call clears the parts that must start at zero). Calls whose
- *     kernels overlap on the GPU race on it: issue them on one stream, or order them.
- *   - A look-back wait that gives up marks the affected outputs NaN.
+ *     call's contents (each call clears, on its stream, the parts that must start at
+ *     zero). Calls whose kernels overlap on the GPU race on it: issue them on one
+ *     stream, or order them.
+ *   - A look-back wait that gives up (about a second without progress) marks the
+ *     affected outputs NaN, and the call still returned RLCA_OK: its timeout record sits
+ *     in the library's array, which no entry point reads. Callers that must detect it
+ *     check the outputs for NaN.
  */
 #define RLCA_NOALLOC_MAX_TILES 32768
 int rlca_gae_noalloc(const float *reward, const float *value, const uint8_t *terminated,

@@ -8,8 +8,8 @@ fallback: if the library is not built, every call raises.
 The functions carry the names of the C entry points (``include/rlca.h``) and take
 torch tensors:
   - per-step tensors: 2-D [N, T], unit stride along T, all with the same row stride;
-    float32 data (or all bfloat16, which selects the _bf16 entry points), uint8 or
-    bool flags;
+    float32 data (or all bfloat16 / all float16, which select the _bf16 / _fp16 entry
+    points), uint8 or bool flags;
   - per-env bootstrap values: float32 [N] (optional);
   - every tensor is on one CUDA device or in pinned host memory (read and written in
     place by the kernels over NVLink-C2C);
@@ -55,10 +55,14 @@ SIGNATURES = {
                                      _P], ctypes.c_int),
 }
 SIGNATURES["rlca_gae_noalloc"] = SIGNATURES["rlca_gae"]
-# bf16-input variants: the same argument list (the data pointers hold bf16).
+# Measurement only (include/rlca_measure.h).
+SIGNATURES["rlca_measure_copy"] = ([_P, ctypes.c_int, _P, ctypes.c_int, _P, ctypes.c_int, _I64,
+                                    ctypes.c_int, _P], ctypes.c_int)
+# 16-bit-input variants: the same argument list (the data pointers hold bf16 or fp16).
 for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
               "rlca_retrace", "rlca_eligibility_trace", "rlca_episodic_prefix_sum"):
     SIGNATURES[_name + "_bf16"] = SIGNATURES[_name]
+    SIGNATURES[_name + "_fp16"] = SIGNATURES[_name]
 # The _ex variants take (workspace, workspace_bytes) before the stream.
 for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
               "rlca_retrace"):
@@ -189,20 +193,30 @@ def workspace_check(workspace: torch.Tensor) -> int:
     return int(lib().rlca_workspace_check(workspace.data_ptr(), _stream(workspace.device)))
 
 
+def _narrow(dd):
+    """The 16-bit data dtype of an allowed-dtype tuple, or None for fp32."""
+    return dd[0] if dd[0] in _NARROW else None
+
+
+# Entry-point suffix of each 16-bit data dtype.
+_NARROW = {torch.bfloat16: "_bf16", torch.float16: "_fp16"}
+
+
 def _data_dtype(t):
-    """Per-step data inputs are all fp32 or all bf16; returns the allowed dtype tuple."""
-    if t.dtype == torch.bfloat16:
-        return (torch.bfloat16,)
+    """Per-step data inputs are all fp32, all bf16 or all fp16; returns the allowed dtype
+    tuple (the first per-step tensor decides)."""
+    if t.dtype in _NARROW:
+        return (t.dtype,)
     return _F32
 
 
-def _call(name, args, workspace, stream, bf16=False):
-    """Call the plain entry point, its _bf16 variant for bf16 inputs, or its _ex variant
-    when a workspace is given."""
-    if bf16:
+def _call(name, args, workspace, stream, narrow=None):
+    """Call the plain entry point, its _bf16 / _fp16 variant for 16-bit inputs (`narrow`,
+    the data dtype), or its _ex variant when a workspace is given."""
+    if narrow is not None:
         if workspace is not None:
-            raise ValueError("the bf16 entry points take no workspace")
-        return getattr(lib(), name + "_bf16")(*args, stream)
+            raise ValueError("the 16-bit input entry points take no workspace")
+        return getattr(lib(), name + _NARROW[narrow])(*args, stream)
     if workspace is None:
         return getattr(lib(), name)(*args, stream)
     if not workspace.is_cuda or workspace.dtype != torch.uint8:
@@ -222,7 +236,7 @@ def rlca_discounted_return(reward, terminated, truncated=None, trunc_value=None,
     returns = g.out(returns, "returns")
     _check("rlca_discounted_return", _call(
         "rlca_discounted_return", (*args, gamma, g.N, g.T, g.ld, returns.data_ptr() or None),
-        workspace, _stream(g.device), dd != _F32))
+        workspace, _stream(g.device), _narrow(dd)))
     return returns
 
 
@@ -237,7 +251,7 @@ def rlca_td_lambda(reward, value, terminated, truncated=None, trunc_value=None,
     targets = g.out(targets, "targets")
     _check("rlca_td_lambda", _call(
         "rlca_td_lambda", (*args, gamma, lam, g.N, g.T, g.ld, targets.data_ptr() or None),
-        workspace, _stream(g.device), dd != _F32))
+        workspace, _stream(g.device), _narrow(dd)))
     return targets
 
 
@@ -255,7 +269,7 @@ def rlca_gae(reward, value, terminated, truncated=None, trunc_value=None, bootst
     _check("rlca_gae", _call(
         "rlca_gae", (*args, gamma, lam, g.N, g.T, g.ld, advantages.data_ptr() or None,
                      returns.data_ptr() or None if returns is not None else None),
-        workspace, _stream(g.device), dd != _F32))
+        workspace, _stream(g.device), _narrow(dd)))
     return advantages, returns
 
 
@@ -278,7 +292,7 @@ def rlca_vtrace(reward, value, log_rho, terminated, truncated=None, trunc_value=
         "rlca_vtrace", (*args, gamma, lam, rho_bar, c_bar, pg_rho_bar, g.N, g.T, g.ld,
                         vs.data_ptr() or None,
                         pg.data_ptr() or None if pg is not None else None),
-        workspace, _stream(g.device), dd != _F32))
+        workspace, _stream(g.device), _narrow(dd)))
     return vs, pg
 
 
@@ -321,7 +335,7 @@ def rlca_retrace(reward, q_taken, expected_q, rho, terminated, truncated=None,
     q_ret = g.out(q_ret, "q_ret")
     _check("rlca_retrace", _call(
         "rlca_retrace", (*args, gamma, lam, g.N, g.T, g.ld, q_ret.data_ptr() or None),
-        workspace, _stream(g.device), dd != _F32))
+        workspace, _stream(g.device), _narrow(dd)))
     return q_ret
 
 
@@ -356,7 +370,7 @@ def rlca_eligibility_trace(x, terminated, truncated=None, init=None, decay=0.95,
     traces = g.out(traces, "traces")
     _check("rlca_eligibility_trace", _call(
         "rlca_eligibility_trace", (*args, decay, g.N, g.T, g.ld, traces.data_ptr() or None),
-        None, _stream(g.device), dd != _F32))
+        None, _stream(g.device), _narrow(dd)))
     return traces
 
 
@@ -369,8 +383,27 @@ def rlca_episodic_prefix_sum(x, terminated, truncated=None, init=None, sums=None
     sums = g.out(sums, "sums")
     _check("rlca_episodic_prefix_sum", _call(
         "rlca_episodic_prefix_sum", (*args, g.N, g.T, g.ld, sums.data_ptr() or None),
-        None, _stream(g.device), dd != _F32))
+        None, _stream(g.device), _narrow(dd)))
     return sums
+
+
+def measure_copy(inputs, flags, outputs, chunks=1):
+    """Measurement only (rlca_measure_copy): one launch that reads every element of the
+    fp32 `inputs` and uint8/bool `flags` and writes every element of the fp32 `outputs`,
+    in the estimator kernels' launch shape (`chunks` 256-element chunks per warp). All
+    tensors are contiguous, on one CUDA device, with the same number of elements."""
+    n = inputs[0].numel()
+    dev = inputs[0].device
+    for t, dts in [(t, _F32) for t in list(inputs) + list(outputs)] + \
+            [(t, _FLAG) for t in flags]:
+        if not t.is_cuda or t.device != dev or not t.is_contiguous() or t.numel() != n:
+            raise ValueError("measure_copy: contiguous tensors of one size on one device")
+        if t.dtype not in dts:
+            raise TypeError(f"measure_copy: dtype {t.dtype} not in {dts}")
+    arr = lambda ts: (ctypes.c_void_p * max(1, len(ts)))(*[t.data_ptr() for t in ts])
+    _check("rlca_measure_copy", lib().rlca_measure_copy(
+        arr(inputs), len(inputs), arr(flags), len(flags), arr(outputs), len(outputs), n,
+        chunks, _stream(dev)))
 
 
 # Short names.

@@ -1,7 +1,8 @@
 """Build librlca.so in-tree with nvcc for sm_103a (GB300).
 
-Each translation unit compiles in its own nvcc process, in parallel, then the objects
-are linked into one shared library with the CUDA runtime linked statically.
+Each translation unit compiles in its own nvcc process, in parallel (the reverse
+estimators once per estimator and input format, the forward scans once per format), then
+the objects are linked into one shared library with the CUDA runtime linked statically.
 Rebuilds only when a source or header is newer than the library.
 """
 from __future__ import annotations
@@ -31,8 +32,26 @@ def nvcc() -> str:
     return path
 
 
+# Sources compiled more than once, one object per set of defines: each reverse
+# estimator in each input format, and the forward scans in each format.
+VARIANTS = {
+    "reverse_unit.cu": [{"RLCA_UNIT_EST": e, "RLCA_UNIT_FMT": f}
+                        for e in range(5) for f in range(3)],
+    "forward_unit.cu": [{"RLCA_UNIT_FMT": f} for f in range(3)],
+}
+
+
 def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def units() -> list[tuple[str, dict]]:
+    """(source, defines) for every object of the library."""
+    out = []
+    for src in sources():
+        for defs in VARIANTS.get(os.path.basename(src), [{}]):
+            out.append((src, defs))
+    return out
 
 
 def _deps() -> list[str]:
@@ -54,16 +73,21 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src: str):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(unit):
+        src, defs = unit
+        tag = "".join(f".{v}" for v in defs.values())
+        obj = os.path.join(BUILD, os.path.basename(src) + tag + ".o")
+        dflags = [f"-D{k}={v}" for k, v in defs.items()]
+        cmd = [cc, *ARCH, *FLAGS, *extra, *dflags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
         return obj, r.stderr
 
-    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        results = list(ex.map(compile_one, sources()))
+    # Longest first: the reverse units dominate the build.
+    todo = sorted(units(), key=lambda u: os.path.basename(u[0]) != "reverse_unit.cu")
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(compile_one, todo))
     if verbose or ptxas_info:
         for _, log in results:
             if log:

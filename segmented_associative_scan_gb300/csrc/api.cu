@@ -10,7 +10,21 @@
 
 namespace {
 
+using rlca::Est;
+using rlca::Fmt;
 using rlca::Params;
+
+// Bytes of one per-step data element in format f.
+size_t in_bytes(Fmt f) { return f == Fmt::kF32 ? 4 : 2; }
+
+// The launch function of reverse estimator E in format f, for validate_and_launch.
+template <Est E>
+auto launcher(Fmt f)
+{
+    return [f](const Params &q, int vec, cudaStream_t s) {
+        return rlca::launch_in_format<E>(f, q, vec, s);
+    };
+}
 
 struct Range {
     uintptr_t lo, hi;
@@ -47,7 +61,7 @@ struct Workspace {
 };
 
 // Where a buffer lives, as the kernels see it.
-enum class Mem { kDevice, kHost, kBad };
+enum class Mem { kDevice, kManaged, kHost, kBad };
 
 // Device memory of the current device (including managed memory) or pinned host memory
 // mapped into the device's address space at the same address (unified addressing).
@@ -63,7 +77,7 @@ Mem classify(const void *ptr, int device)
     case cudaMemoryTypeDevice:
         return a.device == device ? Mem::kDevice : Mem::kBad;
     case cudaMemoryTypeManaged:
-        return Mem::kDevice;
+        return Mem::kManaged;
     case cudaMemoryTypeHost:
         return a.devicePointer == ptr ? Mem::kHost : Mem::kBad;
     default:
@@ -73,7 +87,7 @@ Mem classify(const void *ptr, int device)
 
 // Common validation of inputs, outputs and workspace, then launch.
 // `f32_in` are the required float inputs, `outs` the outputs (outs[0] required).
-// `in_elem`: bytes per element of the per-step data inputs (4 = fp32, 2 = bf16).
+// `in_elem`: bytes per element of the per-step data inputs (4 = fp32, 2 = bf16 or fp16).
 template <typename LaunchFn>
 int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *const *outs,
                         int n_out, Workspace ws, LaunchFn launch, void *stream,
@@ -140,24 +154,29 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
         for (int o = 0; o < n_out; ++o)
             if (outs[o]) bufs[nb++] = outs[o];
         p.host = 0;
+        p.prefetch = 1;
         for (int i = 0; i < nb; ++i) {
             const Mem m = classify(bufs[i], device);
             if (m == Mem::kBad) return RLCA_ERR_MEMORY;
             if (m == Mem::kHost) p.host = 1;
+            if (m != Mem::kDevice) p.prefetch = 0;  // L2 prefetches: device memory only
         }
         // The look-back state lives in device memory (its waits poll it).
-        if (p.ws && classify(p.ws, device) != Mem::kDevice) return RLCA_ERR_MEMORY;
+        if (p.ws) {
+            const Mem m = classify(p.ws, device);
+            if (m != Mem::kDevice && m != Mem::kManaged) return RLCA_ERR_MEMORY;
+        }
     }
 
     // 128-bit loads/stores need 16-byte aligned rows: ld a multiple of 16 bytes of every
-    // array (ld % 4 == 0 for fp32, ld % 8 == 0 for bf16 inputs) and aligned bases.
+    // array (ld % 4 == 0 for fp32, ld % 8 == 0 for 16-bit inputs) and aligned bases.
     bool vec16 = (p.ld % (int64_t)(16 / in_elem)) == 0 && aligned(p.term, 4) &&
                  (!p.trunc || aligned(p.trunc, 4));
     for (int i = 0; i < n_in; ++i) vec16 = vec16 && aligned(f32_in[i], 16);
     for (int o = 0; o < n_out; ++o) vec16 = vec16 && (!outs[o] || aligned(outs[o], 16));
     // 256-bit access to fp32 rows (8 steps per thread in one access) needs 32-byte
     // aligned rows: ld % 8 == 0, fp32 bases 32-byte aligned, flag bases 8-byte aligned
-    // (bf16 inputs keep 128-bit loads; only the fp32 outputs widen then).
+    // (16-bit inputs keep 128-bit loads; only the fp32 outputs widen then).
     bool vec32 = vec16 && (p.ld % 8) == 0 && aligned(p.term, 8) &&
                  (!p.trunc || aligned(p.trunc, 8));
     for (int i = 0; i < n_in; ++i) vec32 = vec32 && (in_elem == 2 || aligned(f32_in[i], 32));
@@ -190,12 +209,12 @@ Params base_params(const float *reward, const uint8_t *term, const uint8_t *trun
     return p;
 }
 
-// bf16 = the per-step data inputs hold bf16 bit patterns (no workspace then).
+// fmt: the format of the per-step data inputs (16-bit formats take no workspace).
 
 int discounted_return(const float *reward, const uint8_t *terminated, const uint8_t *truncated,
                       const float *trunc_value, const float *bootstrap, float gamma, int64_t N,
                       int64_t T, int64_t ld, float *returns, Workspace ws, void *stream,
-                      int spin_limit = 0, int stall = 0, bool bf16 = false)
+                      int spin_limit = 0, int stall = 0, Fmt fmt = Fmt::kF32)
 {
     if (bad_gamma(gamma)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma, 1.f,
@@ -205,16 +224,14 @@ int discounted_return(const float *reward, const uint8_t *terminated, const uint
     p.stall = stall;
     const float *in[] = {reward};
     float *out[] = {returns};
-    if (bf16)
-        return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return_bf16,
-                                   stream, 2);
-    return validate_and_launch(p, in, 1, out, 1, ws, rlca::launch_return, stream);
+    return validate_and_launch(p, in, 1, out, 1, ws, launcher<Est::kReturn>(fmt), stream,
+                               in_bytes(fmt));
 }
 
 int td_lambda(const float *reward, const float *value, const uint8_t *terminated,
               const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
               float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
-              Workspace ws, void *stream, bool bf16 = false)
+              Workspace ws, void *stream, Fmt fmt = Fmt::kF32)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -223,16 +240,14 @@ int td_lambda(const float *reward, const float *value, const uint8_t *terminated
     p.out0 = targets;
     const float *in[] = {reward, value};
     float *out[] = {targets};
-    if (bf16)
-        return validate_and_launch(p, in, 2, out, 1, ws,
-                                   rlca::launch_td_lambda_bf16, stream, 2);
-    return validate_and_launch(p, in, 2, out, 1, ws, rlca::launch_td_lambda, stream);
+    return validate_and_launch(p, in, 2, out, 1, ws, launcher<Est::kTdLambda>(fmt), stream,
+                               in_bytes(fmt));
 }
 
 int gae(const float *reward, const float *value, const uint8_t *terminated,
         const uint8_t *truncated, const float *trunc_value, const float *bootstrap,
         float gamma, float lambda, int64_t N, int64_t T, int64_t ld, float *advantages,
-        float *returns, Workspace ws, void *stream, bool bf16 = false)
+        float *returns, Workspace ws, void *stream, Fmt fmt = Fmt::kF32)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
@@ -242,17 +257,15 @@ int gae(const float *reward, const float *value, const uint8_t *terminated,
     p.out1 = returns;
     const float *in[] = {reward, value};
     float *out[] = {advantages, returns};
-    if (bf16)
-        return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae_bf16,
-                                   stream, 2);
-    return validate_and_launch(p, in, 2, out, 2, ws, rlca::launch_gae, stream);
+    return validate_and_launch(p, in, 2, out, 2, ws, launcher<Est::kGae>(fmt), stream,
+                               in_bytes(fmt));
 }
 
 int vtrace(const float *reward, const float *value, const float *log_rho,
            const uint8_t *terminated, const uint8_t *truncated, const float *trunc_value,
            const float *bootstrap, float gamma, float lambda, float rho_bar, float c_bar,
            float pg_rho_bar, int64_t N, int64_t T, int64_t ld, float *vs,
-           float *pg_advantages, Workspace ws, void *stream, bool bf16 = false)
+           float *pg_advantages, Workspace ws, void *stream, Fmt fmt = Fmt::kF32)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda) || bad_clip(rho_bar) || bad_clip(c_bar) ||
         bad_clip(pg_rho_bar))
@@ -268,17 +281,15 @@ int vtrace(const float *reward, const float *value, const float *log_rho,
     p.out1 = pg_advantages;
     const float *in[] = {reward, value, log_rho};
     float *out[] = {vs, pg_advantages};
-    if (bf16)
-        return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace_bf16,
-                                   stream, 2);
-    return validate_and_launch(p, in, 3, out, 2, ws, rlca::launch_vtrace, stream);
+    return validate_and_launch(p, in, 3, out, 2, ws, launcher<Est::kVtrace>(fmt), stream,
+                               in_bytes(fmt));
 }
 
 int retrace(const float *reward, const float *q_taken, const float *expected_q,
             const float *rho, const uint8_t *terminated, const uint8_t *truncated,
             const float *trunc_value, const float *bootstrap_ev, float gamma, float lambda,
             int64_t N, int64_t T, int64_t ld, float *q_ret, Workspace ws, void *stream,
-            bool bf16 = false)
+            Fmt fmt = Fmt::kF32)
 {
     if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
     Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap_ev, gamma,
@@ -289,10 +300,8 @@ int retrace(const float *reward, const float *q_taken, const float *expected_q,
     p.out0 = q_ret;
     const float *in[] = {reward, q_taken, expected_q, rho};
     float *out[] = {q_ret};
-    if (bf16)
-        return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace_bf16,
-                                   stream, 2);
-    return validate_and_launch(p, in, 4, out, 1, ws, rlca::launch_retrace, stream);
+    return validate_and_launch(p, in, 4, out, 1, ws, launcher<Est::kRetrace>(fmt), stream,
+                               in_bytes(fmt));
 }
 
 int gae_vtrace(const float *reward, const float *value, const float *log_rho,
@@ -325,6 +334,7 @@ int gae_vtrace(const float *reward, const float *value, const float *log_rho,
     auto launch = [&pg](const Params &q, int vec, cudaStream_t s) {
         Params g = pg;  // the same validated shape and memory kind as the V-trace half
         g.host = q.host;
+        g.prefetch = q.prefetch;
         return rlca::launch_gae_vtrace(g, q, vec, s);
     };
     return validate_and_launch(pv, in, 3, out, 4, Workspace{nullptr, 0}, launch, stream);
@@ -368,7 +378,7 @@ int td_lambda_multi(const float *reward, const float *value, const uint8_t *term
 // per-env value carried into the window (nullable); decay >= 0 and finite.
 int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *truncated,
                  const float *init, float decay, int64_t N, int64_t T, int64_t ld, float *out,
-                 void *stream, bool bf16 = false)
+                 void *stream, Fmt fmt = Fmt::kF32)
 {
     if (!std::isfinite(decay) || decay < 0.f) return RLCA_ERR_PARAM;
     Params p = base_params(x, terminated, truncated, nullptr, init, decay, 1.f, N, T, ld);
@@ -377,16 +387,47 @@ int forward_scan(const float *x, const uint8_t *terminated, const uint8_t *trunc
     p.out0 = out;
     const float *in[] = {x};
     float *outs[] = {out};
-    auto launch = [bf16](const Params &q, int vec, cudaStream_t s) {
-        return bf16 ? rlca::launch_forward_bf16(q, vec, s) : rlca::launch_forward(q, vec, s);
+    auto launch = [fmt](const Params &q, int vec, cudaStream_t s) {
+        return rlca::launch_forward_in_format(fmt, q, vec, s);
     };
     return validate_and_launch(p, in, 1, outs, 1, Workspace{nullptr, 0}, launch, stream,
-                               bf16 ? 2 : 4);
+                               in_bytes(fmt));
 }
 
 constexpr Workspace kNoWorkspace{nullptr, 0};
 
 }  // namespace
+
+namespace rlca {
+
+int gae_on_library_workspace(const float *reward, const float *value, const uint8_t *terminated,
+                             const uint8_t *truncated, const float *trunc_value,
+                             const float *bootstrap, float gamma, float lambda, int64_t N,
+                             int64_t T, int64_t ld, float *advantages, float *returns,
+                             void *ws, size_t ws_bytes,
+                             cudaError_t (*prepare)(void *ws, cudaStream_t stream), void *stream)
+{
+    if (bad_gamma(gamma) || bad_lambda(lambda)) return RLCA_ERR_PARAM;
+    Params p = base_params(reward, terminated, truncated, trunc_value, bootstrap, gamma,
+                           lambda, N, T, ld);
+    p.value = value;
+    p.out0 = advantages;
+    p.out1 = returns;
+    const float *in[] = {reward, value};
+    float *out[] = {advantages, returns};
+    // Every check has passed once the launch function runs: only then is the workspace
+    // prepared, on the same stream, right before the kernel.
+    auto launch = [prepare](const Params &q, int vec, cudaStream_t s) {
+        if (q.ws) {
+            const cudaError_t e = prepare(q.ws, s);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_unit<Est::kGae, Fmt::kF32>(q, vec, s);
+    };
+    return validate_and_launch(p, in, 2, out, 2, Workspace{ws, ws_bytes}, launch, stream);
+}
+
+}  // namespace rlca
 
 extern "C" {
 
@@ -569,81 +610,85 @@ int rlca_episodic_prefix_sum(const float *x, const uint8_t *terminated,
     return forward_scan(x, terminated, truncated, init, 1.f, N, T, ld, sums, stream);
 }
 
-// ---- bf16 per-step inputs (bit patterns), fp32 bootstrap values and outputs.
+// ---- 16-bit per-step inputs (bf16 or fp16 bit patterns), fp32 bootstrap values and
+// outputs: the same seven entry points for each format, SUFFIX _bf16 or _fp16.
 
-#define RLCA_BF(p) reinterpret_cast<const float *>(p)
+#define RLCA_IN(p) reinterpret_cast<const float *>(p)
+#define RLCA_NARROW_ENTRY_POINTS(SUFFIX, FMT)                                                   \
+    int rlca_discounted_return##SUFFIX(const uint16_t *reward, const uint8_t *terminated,       \
+                                       const uint8_t *truncated, const uint16_t *trunc_value,   \
+                                       const float *bootstrap, float gamma, int64_t N,          \
+                                       int64_t T, int64_t ld, float *returns, void *stream)     \
+    {                                                                                           \
+        return discounted_return(RLCA_IN(reward), terminated, truncated, RLCA_IN(trunc_value), \
+                                 bootstrap, gamma, N, T, ld, returns, kNoWorkspace, stream, 0, \
+                                 0, FMT);                                                       \
+    }                                                                                           \
+    int rlca_td_lambda##SUFFIX(const uint16_t *reward, const uint16_t *value,                   \
+                               const uint8_t *terminated, const uint8_t *truncated,             \
+                               const uint16_t *trunc_value, const float *bootstrap,             \
+                               float gamma, float lambda, int64_t N, int64_t T, int64_t ld,     \
+                               float *targets, void *stream)                                    \
+    {                                                                                           \
+        return td_lambda(RLCA_IN(reward), RLCA_IN(value), terminated, truncated,                \
+                         RLCA_IN(trunc_value), bootstrap, gamma, lambda, N, T, ld, targets,     \
+                         kNoWorkspace, stream, FMT);                                            \
+    }                                                                                           \
+    int rlca_gae##SUFFIX(const uint16_t *reward, const uint16_t *value,                         \
+                         const uint8_t *terminated, const uint8_t *truncated,                   \
+                         const uint16_t *trunc_value, const float *bootstrap, float gamma,      \
+                         float lambda, int64_t N, int64_t T, int64_t ld, float *advantages,     \
+                         float *returns, void *stream)                                          \
+    {                                                                                           \
+        return gae(RLCA_IN(reward), RLCA_IN(value), terminated, truncated,                      \
+                   RLCA_IN(trunc_value), bootstrap, gamma, lambda, N, T, ld, advantages,        \
+                   returns, kNoWorkspace, stream, FMT);                                         \
+    }                                                                                           \
+    int rlca_vtrace##SUFFIX(const uint16_t *reward, const uint16_t *value,                      \
+                            const uint16_t *log_rho, const uint8_t *terminated,                 \
+                            const uint8_t *truncated, const uint16_t *trunc_value,              \
+                            const float *bootstrap, float gamma, float lambda, float rho_bar,   \
+                            float c_bar, float pg_rho_bar, int64_t N, int64_t T, int64_t ld,    \
+                            float *vs, float *pg_advantages, void *stream)                      \
+    {                                                                                           \
+        return vtrace(RLCA_IN(reward), RLCA_IN(value), RLCA_IN(log_rho), terminated,           \
+                      truncated, RLCA_IN(trunc_value), bootstrap, gamma, lambda, rho_bar,       \
+                      c_bar, pg_rho_bar, N, T, ld, vs, pg_advantages, kNoWorkspace, stream,     \
+                      FMT);                                                                     \
+    }                                                                                           \
+    int rlca_retrace##SUFFIX(const uint16_t *reward, const uint16_t *q_taken,                   \
+                             const uint16_t *expected_q, const uint16_t *rho,                   \
+                             const uint8_t *terminated, const uint8_t *truncated,               \
+                             const uint16_t *trunc_value, const float *bootstrap_ev,            \
+                             float gamma, float lambda, int64_t N, int64_t T, int64_t ld,       \
+                             float *q_ret, void *stream)                                        \
+    {                                                                                           \
+        return retrace(RLCA_IN(reward), RLCA_IN(q_taken), RLCA_IN(expected_q), RLCA_IN(rho),   \
+                       terminated, truncated, RLCA_IN(trunc_value), bootstrap_ev, gamma,        \
+                       lambda, N, T, ld, q_ret, kNoWorkspace, stream, FMT);                     \
+    }                                                                                           \
+    int rlca_eligibility_trace##SUFFIX(const uint16_t *x, const uint8_t *terminated,            \
+                                       const uint8_t *truncated, const float *init,             \
+                                       float decay, int64_t N, int64_t T, int64_t ld,           \
+                                       float *traces, void *stream)                             \
+    {                                                                                           \
+        return forward_scan(RLCA_IN(x), terminated, truncated, init, decay, N, T, ld, traces,   \
+                            stream, FMT);                                                       \
+    }                                                                                           \
+    int rlca_episodic_prefix_sum##SUFFIX(const uint16_t *x, const uint8_t *terminated,          \
+                                         const uint8_t *truncated, const float *init,           \
+                                         int64_t N, int64_t T, int64_t ld, float *sums,         \
+                                         void *stream)                                          \
+    {                                                                                           \
+        return forward_scan(RLCA_IN(x), terminated, truncated, init, 1.f, N, T, ld, sums,       \
+                            stream, FMT);                                                       \
+    }
 
-int rlca_discounted_return_bf16(const uint16_t *reward, const uint8_t *terminated,
-                                const uint8_t *truncated, const uint16_t *trunc_value,
-                                const float *bootstrap, float gamma, int64_t N, int64_t T,
-                                int64_t ld, float *returns, void *stream)
-{
-    return discounted_return(RLCA_BF(reward), terminated, truncated, RLCA_BF(trunc_value),
-                             bootstrap, gamma, N, T, ld, returns, kNoWorkspace, stream, 0, 0,
-                             true);
-}
+RLCA_NARROW_ENTRY_POINTS(_bf16, Fmt::kBF16)
+RLCA_NARROW_ENTRY_POINTS(_fp16, Fmt::kF16)
 
-int rlca_td_lambda_bf16(const uint16_t *reward, const uint16_t *value,
-                        const uint8_t *terminated, const uint8_t *truncated,
-                        const uint16_t *trunc_value, const float *bootstrap, float gamma,
-                        float lambda, int64_t N, int64_t T, int64_t ld, float *targets,
-                        void *stream)
-{
-    return td_lambda(RLCA_BF(reward), RLCA_BF(value), terminated, truncated,
-                     RLCA_BF(trunc_value), bootstrap, gamma, lambda, N, T, ld, targets,
-                     kNoWorkspace, stream, true);
-}
-
-int rlca_gae_bf16(const uint16_t *reward, const uint16_t *value, const uint8_t *terminated,
-                  const uint8_t *truncated, const uint16_t *trunc_value, const float *bootstrap,
-                  float gamma, float lambda, int64_t N, int64_t T, int64_t ld,
-                  float *advantages, float *returns, void *stream)
-{
-    return gae(RLCA_BF(reward), RLCA_BF(value), terminated, truncated, RLCA_BF(trunc_value),
-               bootstrap, gamma, lambda, N, T, ld, advantages, returns, kNoWorkspace, stream,
-               true);
-}
-
-int rlca_vtrace_bf16(const uint16_t *reward, const uint16_t *value, const uint16_t *log_rho,
-                     const uint8_t *terminated, const uint8_t *truncated,
-                     const uint16_t *trunc_value, const float *bootstrap, float gamma,
-                     float lambda, float rho_bar, float c_bar, float pg_rho_bar, int64_t N,
-                     int64_t T, int64_t ld, float *vs, float *pg_advantages, void *stream)
-{
-    return vtrace(RLCA_BF(reward), RLCA_BF(value), RLCA_BF(log_rho), terminated, truncated,
-                  RLCA_BF(trunc_value), bootstrap, gamma, lambda, rho_bar, c_bar, pg_rho_bar, N,
-                  T, ld, vs, pg_advantages, kNoWorkspace, stream, true);
-}
-
-int rlca_retrace_bf16(const uint16_t *reward, const uint16_t *q_taken,
-                      const uint16_t *expected_q, const uint16_t *rho,
-                      const uint8_t *terminated, const uint8_t *truncated,
-                      const uint16_t *trunc_value, const float *bootstrap_ev, float gamma,
-                      float lambda, int64_t N, int64_t T, int64_t ld, float *q_ret,
-                      void *stream)
-{
-    return retrace(RLCA_BF(reward), RLCA_BF(q_taken), RLCA_BF(expected_q), RLCA_BF(rho),
-                   terminated, truncated, RLCA_BF(trunc_value), bootstrap_ev, gamma, lambda, N,
-                   T, ld, q_ret, kNoWorkspace, stream, true);
-}
-
-int rlca_eligibility_trace_bf16(const uint16_t *x, const uint8_t *terminated,
-                                const uint8_t *truncated, const float *init, float decay,
-                                int64_t N, int64_t T, int64_t ld, float *traces, void *stream)
-{
-    return forward_scan(RLCA_BF(x), terminated, truncated, init, decay, N, T, ld, traces, stream,
-                        true);
-}
-
-int rlca_episodic_prefix_sum_bf16(const uint16_t *x, const uint8_t *terminated,
-                                  const uint8_t *truncated, const float *init, int64_t N,
-                                  int64_t T, int64_t ld, float *sums, void *stream)
-{
-    return forward_scan(RLCA_BF(x), terminated, truncated, init, 1.f, N, T, ld, sums, stream,
-                        true);
-}
-
-#undef RLCA_BF
+#undef RLCA_NARROW_ENTRY_POINTS
+#undef RLCA_IN
 
 int rlca_testing_lookback_stall(const float *reward, const uint8_t *terminated, int64_t N,
                                 int64_t T, float *returns, void *workspace,

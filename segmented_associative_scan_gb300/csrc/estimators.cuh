@@ -70,7 +70,10 @@ struct Params {
     int spin_limit;   // consecutive empty polls of a later tile before giving up
     int stall;        // testing only: nonzero = tiles never publish their state
     int forward;      // host-side only: a forward scan (truncation needs no values)
-    int host;         // host-side only: some data live in pinned host memory
+    int host;         // some data live in pinned host memory (picks the kernel)
+    int prefetch;     // every buffer is plain device memory: L2 prefetches allowed
+    int pf_first;     // pipelined warp rows: steps prefetched into L2 before the wait
+    int pf_ahead;     // pipelined warp rows: chunk s - pf_ahead prefetched at chunk s (0: off)
     MultiLambda multi;  // fused TD(lambda) only
 };
 
@@ -111,6 +114,26 @@ template <typename TIn>
 __device__ __forceinline__ const TIn *in_row(const float *base, int64_t off)
 {
     return reinterpret_cast<const TIn *>(base) + off;
+}
+
+// Columns [t_lo, t_hi) of one row of every per-step array estimator E streams in (data
+// and flags; the sparse truncation values are left out) prefetched into L2. A kernel
+// issues this before its grid dependency wait, so the reads of its first rows overlap
+// the tail of the previous kernel in the stream. Only when every buffer is plain device
+// memory (not pinned host or managed memory).
+template <Est E, bool TRUNC, typename TIn = float>
+__device__ __forceinline__ void prefetch_row(const Params &p, int64_t row, int t_lo, int t_hi)
+{
+    using Tr = EstTraits<E>;
+    if (!p.prefetch || row >= p.N || t_hi <= t_lo) return;
+    const int64_t off = row * p.ld + t_lo;
+    const int64_t n = t_hi - t_lo;
+    prefetch_l2(in_row<TIn>(p.reward, off), n * (int64_t)sizeof(TIn));
+    if (Tr::kValue) prefetch_l2(in_row<TIn>(p.value, off), n * (int64_t)sizeof(TIn));
+    if (Tr::kAux) prefetch_l2(in_row<TIn>(p.aux, off), n * (int64_t)sizeof(TIn));
+    if (Tr::kRho) prefetch_l2(in_row<TIn>(p.rho, off), n * (int64_t)sizeof(TIn));
+    prefetch_l2(p.term + off, n);
+    if (TRUNC) prefetch_l2(p.trunc + off, n);
 }
 
 // Successor of item ITEMS-1: the next lane's first item, or (lane 31) a direct load.

@@ -20,24 +20,20 @@
 
 namespace rlca {
 
-// One chunk: A at the step before the chunk is `carry_in`; `prev_ended` says whether the
-// step before lane 0's first step ended an episode. Returns A at the chunk's last step;
-// *last_ended gets whether that step ended an episode.
-template <int ITEMS, int VEC, bool TRUNC, typename TIn = float>
-__device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int t0, bool active,
-                                               float carry_in, bool prev_ended,
-                                               bool *last_ended)
+// One loaded chunk of a warp: x (ITEMS steps per lane, zero past the row's end), `ended`
+// (bit j: step t0+j terminated or truncated) and `valid` (bit j: step t0+j exists). A at
+// the step before the chunk is `carry_in`; `prev_ended` says whether the step before
+// lane 0's first step ended an episode. Returns A at the chunk's last step; *last_ended
+// gets whether that step ended an episode. Every lane of the warp calls this.
+template <int ITEMS, int VEC, typename TIn = float>
+__device__ __forceinline__ float forward_chunk_scan(const Params &p, int64_t row, int t0,
+                                                    bool active, float (&x)[ITEMS],
+                                                    unsigned ended, unsigned valid,
+                                                    float carry_in, bool prev_ended,
+                                                    bool *last_ended)
 {
     const int lane = threadIdx.x & 31;
-    const int T = p.T;
-    const int Te = active ? T : 0;
     const int64_t off = active ? row * p.ld : 0;
-
-    float x[ITEMS];
-    load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, x);
-    const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
-                                 : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
-    const unsigned valid = valid_items<ITEMS>(t0, Te);
 
     // Item j starts afresh when step t0+j-1 ended an episode; the row's first step resets
     // too and takes the carried-in value as its own term.
@@ -49,9 +45,6 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
         if (p.boot) x[0] = fmaf(p.gamma, __ldg(p.boot + row), x[0]);
     }
     reset &= all_items<ITEMS>();
-#pragma unroll
-    for (int j = 0; j < ITEMS; ++j)
-        if (!((valid >> j) & 1u)) x[j] = 0.f;
 
     // Composite of the lane's items in time order, e_{ITEMS-1} o ... o e_0.
     const float decay = p.gamma;
@@ -83,13 +76,40 @@ __device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int
     return affine_apply(whole, carry_in);
 }
 
+// The same, loading the chunk first (ragged and inactive chunks allowed).
+template <int ITEMS, int VEC, bool TRUNC, typename TIn = float>
+__device__ __forceinline__ float forward_chunk(const Params &p, int64_t row, int t0, bool active,
+                                               float carry_in, bool prev_ended,
+                                               bool *last_ended)
+{
+    const int T = p.T;
+    const int Te = active ? T : 0;
+    const int64_t off = active ? row * p.ld : 0;
+    float x[ITEMS];
+    load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, x);
+    const unsigned ended = TRUNC ? load_flag_bits_or<ITEMS, VEC>(p.term + off, p.trunc + off, t0, Te)
+                                 : load_flag_bits<ITEMS, VEC>(p.term + off, t0, Te);
+    const unsigned valid = valid_items<ITEMS>(t0, Te);
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j)
+        if (!((valid >> j) & 1u)) x[j] = 0.f;
+    return forward_chunk_scan<ITEMS, VEC, TIn>(p, row, t0, active, x, ended, valid, carry_in,
+                                               prev_ended, last_ended);
+}
+
 template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4, typename TIn = float>
 __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params p)
 {
-    grid_dependency_sync();
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    // x and the flags are what the discounted return streams in, too.
+    if (p.segs == 1) {
+        prefetch_warp_rows<Est::kReturn, TRUNC, TIn>(p, job, p.T);
+    } else if (lane == 0) {
+        prefetch_row<Est::kReturn, TRUNC, TIn>(p, job, 0, p.T < 1024 ? p.T : 1024);
+    }
+    grid_dependency_sync();
     bool last_ended = false;
     if (p.segs == 1) {
         const int local_row = lane / p.chunks_per_row;
@@ -105,6 +125,63 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
             carry = forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, job, s * CH + lane * ITEMS, true,
                                                           carry, last_ended, &last_ended);
     }
+}
+
+// ------------------------------------------------------- pipelined warp rows, forward
+
+// One row per warp, walked in chunks of 32 * ITEMS steps from the first to the last
+// with the next chunks' loads in flight: before a chunk is scanned, the raw words of the
+// DEPTH chunks after it have been requested into registers, so the warp's HBM reads
+// overlap its own scans and stores (the forward mirror of warp_pipe_row). L2 prefetch:
+// the first pf_first steps before the grid dependency wait, and at chunk s the chunk
+// s + pf_ahead (0: none). Full chunks go through the pipeline; a ragged last chunk is
+// loaded plainly at the end. Needs 16-byte aligned rows (VEC >= 1).
+template <int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4, typename TIn = float,
+          int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_forward_pipe_kernel(const Params p)
+{
+    static_assert(DEPTH == 1 || DEPTH == 2, "one or two chunks in flight");
+    static_assert(VEC & kVec16, "raw chunks are read with vector loads");
+    constexpr Est E = Est::kReturn;  // streams x (as reward) and the flags, nothing else
+    constexpr int CH = 32 * ITEMS;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (lane == 0) prefetch_row<E, TRUNC, TIn>(p, row, 0, p.T < p.pf_first ? p.T : p.pf_first);
+    grid_dependency_sync();
+    if (row >= p.N) return;  // the whole warp leaves together
+    const int64_t off = row * p.ld;
+    const int full = p.T / CH;
+    float carry = 0.f;
+    bool ended_before = false;
+    RawChunk<E, ITEMS, TIn> w0, w1;
+    if (full > 0) load_raw<E, ITEMS, VEC, TRUNC>(p, off, lane * ITEMS, lane, w0);
+    if (DEPTH == 2 && full > 1) load_raw<E, ITEMS, VEC, TRUNC>(p, off, CH + lane * ITEMS, lane, w1);
+    for (int s = 0; s < full; ++s) {
+        const int t0 = s * CH + lane * ITEMS;
+        if (lane == 0 && p.pf_ahead > 0 && (s + p.pf_ahead) * CH < p.T) {
+            const int lo = (s + p.pf_ahead) * CH;
+            prefetch_row<E, TRUNC, TIn>(p, row, lo, lo + CH < p.T ? lo + CH : p.T);
+        }
+        float x[ITEMS];
+        widen_words<TIn>(w0.r, x);
+        unsigned ended = 0;
+#pragma unroll
+        for (int k = 0; k < ITEMS / 4; ++k)
+            ended |= nonzero_bytes(TRUNC ? (w0.term[k] | w0.trunc[k]) : w0.term[k]) << (4 * k);
+        if (DEPTH == 2) {
+            w0 = w1;
+            if (s + 2 < full)
+                load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s + 2) * CH + lane * ITEMS, lane, w1);
+        } else if (s + 1 < full) {
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s + 1) * CH + lane * ITEMS, lane, w0);
+        }
+        carry = forward_chunk_scan<ITEMS, VEC, TIn>(p, row, t0, true, x, ended,
+                                                    all_items<ITEMS>(), carry, ended_before,
+                                                    &ended_before);
+    }
+    if (full * CH < p.T)
+        forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, row, full * CH + lane * ITEMS, true, carry,
+                                              ended_before, &ended_before);
 }
 
 // ------------------------------------------------------------------ CTA tiles
@@ -201,8 +278,16 @@ template <int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL, typename TIn = floa
 __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
-    grid_dependency_sync();
     constexpr int TILE = NT * ITEMS;
+    // x and the flags (the discounted return's arrays); the row loop starts at tile 0.
+    if (TL == Tiling::kRows) {
+        if ((int)threadIdx.x < p.rows_per_tile)
+            prefetch_row<Est::kReturn, TRUNC, TIn>(
+                p, (int64_t)blockIdx.x * p.rows_per_tile + threadIdx.x, 0, p.T);
+    } else if (threadIdx.x == 0) {
+        prefetch_row<Est::kReturn, TRUNC, TIn>(p, blockIdx.x, 0, p.T < TILE ? p.T : TILE);
+    }
+    grid_dependency_sync();
     if (TL == Tiling::kRows) {
         const int local_row = threadIdx.x / p.chunks_per_row;
         const int chunk = threadIdx.x - local_row * p.chunks_per_row;
@@ -219,10 +304,14 @@ __global__ void __launch_bounds__(NT) credit_forward_tile_kernel(const Params p)
         const int64_t row = blockIdx.x;
         float carry = 0.f;
         bool ended = false;
-        for (int s = 0; s < p.segs; ++s)
+        for (int s = 0; s < p.segs; ++s) {
+            if (threadIdx.x == 0 && s + 1 < p.segs)
+                prefetch_row<Est::kReturn, TRUNC, TIn>(
+                    p, row, (s + 1) * TILE, (s + 2) * TILE < p.T ? (s + 2) * TILE : p.T);
             carry = forward_tile<NT, ITEMS, VEC, TRUNC, TIn>(p, row,
                                                              s * TILE + threadIdx.x * ITEMS, true,
                                                              carry, ended, &ended, sm, s & 1);
+        }
     }
 }
 

@@ -1,16 +1,44 @@
-// Forward scans (eligibility traces, episodic prefix sums) in a translation unit of
-// their own, walked from the first step to the last.
+// Forward scans (eligibility traces, episodic prefix sums), walked from the first step
+// to the last, in one input format: compiled once per format with RLCA_UNIT_FMT (the Fmt
+// value) set by the build.
 #include "forward.cuh"
 #include "launch.cuh"
 
+#if !defined(RLCA_UNIT_FMT)
+#error "forward_unit.cu is compiled with -DRLCA_UNIT_FMT=<0..2>"
+#endif
+
 namespace rlca {
 
-// Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows: CTA tiles of
-// 1024 steps (whole rows, or a row walked tile by tile), which load a whole tile at once.
+// Pipelined forward warp rows: chunks in flight in registers (1 or 2), L2 prefetch
+// before the wait (steps) and ahead of the walk (chunks), and the rows they take
+// (pipe_from < T <= 1024, device memory, 16-byte aligned rows).
+struct ForwardPipe {
+    int depth, first, ahead, pipe_from;
+};
+constexpr ForwardPipe kForwardPipe = {1, 256, 0, 256};
+
+// Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows up to one CTA
+// tile in device memory with 16-byte aligned rows: a warp per row with its next chunk's
+// loads in flight. Otherwise CTA tiles of 1024 steps (whole rows, or a row walked tile by
+// tile), which load a whole tile at once.
 template <int VEC, bool TRUNC, typename TIn = float>
 cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * kItems;
+    if constexpr ((VEC & kVec16) != 0) {
+        if (p.T > kForwardPipe.pipe_from && p.T <= kTile && !p.host) {
+            p.segs = (p.T + CH - 1) / CH;
+            p.chunks_per_row = CH / kItems;
+            p.rows_per_tile = 1;
+            p.pf_first = kForwardPipe.first;
+            p.pf_ahead = kForwardPipe.ahead;
+            const unsigned grid = (unsigned)((p.N + kWarpsPerCta - 1) / kWarpsPerCta);
+            return launch_pdl(credit_forward_pipe_kernel<kItems, kVec16, TRUNC,
+                                                         kForwardPipe.depth, kWarpsPerCta, TIn>,
+                              grid, 32 * kWarpsPerCta, 0, stream, p);
+        }
+    }
     if (p.T <= CH) {
         const int t_pad = (p.T + kItems - 1) / kItems * kItems;
         p.segs = 1;
@@ -43,9 +71,10 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         (unsigned)p.N, kThreads, 0, stream, p);
 }
 
-template <typename TIn>
-cudaError_t launch_forward_typed(const Params &p_in, int vec, cudaStream_t stream)
+template <Fmt F>
+cudaError_t launch_forward_unit(const Params &p_in, int vec, cudaStream_t stream)
 {
+    using TIn = typename FmtType<F>::type;
     Params p = p_in;
     // decay^kItems in the kernel's multiply order, for the per-lane composite.
     p.beta_pow = p.gamma;
@@ -59,14 +88,7 @@ cudaError_t launch_forward_typed(const Params &p_in, int vec, cudaStream_t strea
     });
 }
 
-cudaError_t launch_forward(const Params &p, int vec, cudaStream_t stream)
-{
-    return launch_forward_typed<float>(p, vec, stream);
-}
-
-cudaError_t launch_forward_bf16(const Params &p, int vec, cudaStream_t stream)
-{
-    return launch_forward_typed<uint16_t>(p, vec, stream);
-}
+template cudaError_t launch_forward_unit<static_cast<Fmt>(RLCA_UNIT_FMT)>(const Params &, int,
+                                                                       cudaStream_t);
 
 }  // namespace rlca

@@ -234,11 +234,44 @@ __device__ __forceinline__ void grid_dependency_sync()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// What a CTA of a tile kernel reads first, prefetched into L2 before its grid dependency
+// wait: its whole rows (kRows, kRow) or the first tile it scans (kRowLoop: the row's
+// last tile). One thread per row. Look-back tiles learn their tile only after the wait.
+template <Est E, bool TRUNC, typename TIn, Tiling TL, int TILE>
+__device__ __forceinline__ void prefetch_cta_rows(const Params &p)
+{
+    if (TL == Tiling::kRows) {
+        if ((int)threadIdx.x < p.rows_per_tile)
+            prefetch_row<E, TRUNC, TIn>(p, (int64_t)blockIdx.x * p.rows_per_tile + threadIdx.x,
+                                        0, p.T);
+    } else if (TL == Tiling::kRow) {
+        if (threadIdx.x == 0) prefetch_row<E, TRUNC, TIn>(p, blockIdx.x, 0, p.T);
+    } else if (TL == Tiling::kRowLoop) {
+        if (threadIdx.x == 0)
+            prefetch_row<E, TRUNC, TIn>(p, blockIdx.x, (p.segs - 1) * TILE, p.T);
+    }
+}
+
+// The same for a warp that owns rows_per_tile whole rows (segs == 1; lane i takes row
+// row0 + i) or walks one row (the last `steps` steps, which it scans first).
+template <Est E, bool TRUNC, typename TIn>
+__device__ __forceinline__ void prefetch_warp_rows(const Params &p, int64_t job, int steps)
+{
+    const int lane = threadIdx.x & 31;
+    if (p.segs == 1) {
+        if (lane < p.rows_per_tile)
+            prefetch_row<E, TRUNC, TIn>(p, job * p.rows_per_tile + lane, 0, p.T);
+    } else if (lane == 0) {
+        prefetch_row<E, TRUNC, TIn>(p, job, p.T > steps ? p.T - steps : 0, p.T);
+    }
+}
+
 template <Est E, int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL, int MINB = 1,
           typename TIn = float>
 __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
+    prefetch_cta_rows<E, TRUNC, TIn, TL, NT * ITEMS>(p);
     grid_dependency_sync();
     constexpr int TILE = NT * ITEMS;
     if (TL == Tiling::kRows) {
@@ -256,9 +289,12 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
     } else if (TL == Tiling::kRowLoop) {
         const int64_t row = blockIdx.x;
         float carry = 0.f;
-        for (int s = p.segs - 1; s >= 0; --s)
+        for (int s = p.segs - 1; s >= 0; --s) {
+            if (threadIdx.x == 0 && s > 0)  // the next tile's reads overlap this tile
+                prefetch_row<E, TRUNC, TIn>(p, row, (s - 1) * TILE, s * TILE);
             carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn>(
                 p, row, s * TILE + threadIdx.x * ITEMS, true, carry, sm, s & 1);
+        }
     } else {
         LookbackHeader *h = static_cast<LookbackHeader *>(p.ws);
         if (threadIdx.x == 0) {
@@ -298,6 +334,7 @@ template <int NT, int ITEMS, int VEC, bool TRUNC, Tiling TL>
 __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
 {
     __shared__ ScanSmem<NT> sm;
+    prefetch_cta_rows<Est::kTdLambda, TRUNC, float, TL, NT * ITEMS>(p);
     grid_dependency_sync();
     constexpr int TILE = NT * ITEMS;
     int call = 0;
@@ -329,7 +366,11 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
         tile(blockIdx.x, threadIdx.x * ITEMS, true, carry);
     } else {
         const int64_t row = blockIdx.x;
-        for (int s = p.segs - 1; s >= 0; --s) tile(row, s * TILE + threadIdx.x * ITEMS, true, carry);
+        for (int s = p.segs - 1; s >= 0; --s) {
+            if (threadIdx.x == 0 && s > 0)
+                prefetch_row<Est::kTdLambda, TRUNC>(p, row, (s - 1) * TILE, s * TILE);
+            tile(row, s * TILE + threadIdx.x * ITEMS, true, carry);
+        }
     }
 }
 
@@ -339,10 +380,11 @@ __global__ void __launch_bounds__(NT) credit_td_multi_kernel(const Params p)
 template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4>
 __global__ void __launch_bounds__(32 * WARPS) credit_td_multi_warp_kernel(const Params p)
 {
-    grid_dependency_sync();
     constexpr Est E = Est::kTdLambda;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    prefetch_warp_rows<E, TRUNC, float>(p, job, p.T);
+    grid_dependency_sync();
     const int local_row = lane / p.chunks_per_row;
     const int chunk = lane - local_row * p.chunks_per_row;
     const int64_t row = job * p.rows_per_tile + local_row;
@@ -383,6 +425,7 @@ __global__ void __launch_bounds__(NT, MINB) credit_gae_vtrace_kernel(const Param
                                                                       const Params pv)
 {
     __shared__ ScanSmem<NT> sm;
+    prefetch_cta_rows<Est::kVtrace, TRUNC, float, TL, NT * ITEMS>(pv);
     grid_dependency_sync();
     constexpr int TILE = NT * ITEMS;
     auto tile = [&](int64_t row, int t0, bool active, float (&carry)[2], int buf) {
@@ -403,8 +446,11 @@ __global__ void __launch_bounds__(NT, MINB) credit_gae_vtrace_kernel(const Param
         tile(blockIdx.x, threadIdx.x * ITEMS, true, carry, 0);
     } else {
         const int64_t row = blockIdx.x;
-        for (int s = pv.segs - 1; s >= 0; --s)
+        for (int s = pv.segs - 1; s >= 0; --s) {
+            if (threadIdx.x == 0 && s > 0)
+                prefetch_row<Est::kVtrace, TRUNC>(pv, row, (s - 1) * TILE, s * TILE);
             tile(row, s * TILE + threadIdx.x * ITEMS, true, carry, 0);
+        }
     }
 }
 
@@ -415,9 +461,10 @@ template <int ITEMS, int VEC, bool TRUNC, int WARPS = 4, int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_gae_vtrace_warp_kernel(
     const Params pg, const Params pv)
 {
-    grid_dependency_sync();
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    prefetch_warp_rows<Est::kVtrace, TRUNC, float>(pv, job, pv.T);
+    grid_dependency_sync();
     const int local_row = lane / pv.chunks_per_row;
     const int chunk = lane - local_row * pv.chunks_per_row;
     const int64_t row = job * pv.rows_per_tile + local_row;
@@ -496,10 +543,11 @@ template <Est E, int ITEMS, int VEC, bool TRUNC, int WARPS = 4, typename TIn = f
           int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Params p)
 {
-    grid_dependency_sync();
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    prefetch_warp_rows<E, TRUNC, TIn>(p, job, 1024);
+    grid_dependency_sync();
     if (p.segs == 1) {
         const int local_row = lane / p.chunks_per_row;
         const int chunk = lane - local_row * p.chunks_per_row;
@@ -544,6 +592,9 @@ __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan
         load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w1);
     for (; s >= 0; --s) {
         const int t0 = s * CH + lane * ITEMS;
+        if (lane == 0 && p.pf_ahead > 0 && s >= p.pf_ahead)  // beyond the registers' reach
+            prefetch_row<E, TRUNC, TIn>(p, row, (s - p.pf_ahead) * CH,
+                                        (s - p.pf_ahead + 1) * CH);
         Chunk<ITEMS> c;
         unpack_raw<E, ITEMS, TRUNC>(w0, p.T, t0, lane, c);
         if (DEPTH == 2) {
@@ -563,8 +614,10 @@ template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4,
           typename TIn = float, int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(const Params p)
 {
-    grid_dependency_sync();
     const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0)  // the row's last pf_first steps, scanned first
+        prefetch_row<E, TRUNC, TIn>(p, row, p.T > p.pf_first ? p.T - p.pf_first : 0, p.T);
+    grid_dependency_sync();
     if (row >= p.N) return;  // the whole warp leaves together
     float carry = 0.f;
     warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, TIn>(p, row, [&](int t0, Chunk<ITEMS> &c) {
@@ -578,8 +631,10 @@ template <int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4, int MINB = 0
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_td_multi_pipe_kernel(const Params p)
 {
     constexpr Est E = Est::kTdLambda;
-    grid_dependency_sync();
     const int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0)
+        prefetch_row<E, TRUNC, float>(p, row, p.T > p.pf_first ? p.T - p.pf_first : 0, p.T);
+    grid_dependency_sync();
     if (row >= p.N) return;
     float carry[kMaxLambdas] = {0.f, 0.f, 0.f, 0.f};
     warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, float>(p, row, [&](int t0, Chunk<ITEMS> &c) {

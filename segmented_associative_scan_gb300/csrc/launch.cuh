@@ -81,7 +81,7 @@ inline int sm_count()
 // look-back is 1.9x faster, at [512, 16384] 1.1x slower, at [2048, 4096] 1.3x slower).
 inline bool lookback_pays(int64_t N) { return N < 2 * (int64_t)sm_count(); }
 
-// fp32 inputs (bf16: launch_estimator_bf16 below). Measured on GB300 (CUDA-event timing,
+// fp32 inputs (16-bit: launch_estimator_narrow below). Measured on GB300 (CUDA-event timing,
 // inputs rotated past L2): rows of at most one warp chunk (256 steps) go to warp-owned
 // rows, which need no CTA barrier; up to one CTA tile (1024 steps) the CTA tile kernel,
 // which loads a whole row at once, wins for every estimator but GAE with truncation (or
@@ -166,6 +166,11 @@ template <Est E, int VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
 cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * ITEMS;
+    if (ITEMS != kItems) {  // the constant beta to the power of the steps per lane
+        const float beta = E == Est::kReturn ? p.gamma : p.gamma_lambda;
+        p.beta_pow = beta;
+        for (int i = 1; i < ITEMS; ++i) p.beta_pow = beta * p.beta_pow;
+    }
     int64_t jobs;
     if (p.T <= CH) {
         const int t_pad = (p.T + ITEMS - 1) / ITEMS * ITEMS;
@@ -185,12 +190,61 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
                       grid, 32 * kWarpsPerCta, 0, stream, p);
 }
 
+// L2 prefetch of the pipelined warp rows: steps prefetched before the grid dependency
+// wait (from the row's end, where the walk starts) and how many chunks ahead of the scan
+// a chunk is prefetched inside the walk (0: none), beyond the chunks whose loads the
+// registers already hold. Measured on GB300 at [4096, 1024], us per launch, for (before
+// the wait, ahead) = (0, 0) / (256, 0) / (256, 2) / (1024, 0) / (0, 2) / (512, 3):
+//   GAE fp32 12.86 / 12.30 / 12.76 / 14.29 / 13.23 / 12.94;
+//   GAE bf16 10.84 / 10.85 / 12.29 / 12.98 / 12.04 / 11.98;
+//   fused TD(lambda), 3 lambdas, 15.63 / 14.82 / 15.08 / 16.49 / 15.72 / 14.39;
+//   return bf16 7.79 / 7.50 / 8.28 / 7.10 / 8.49 / 7.35;
+//   TD(lambda) bf16 8.58 / 7.76 / 9.04 / 8.15 / 8.98 / 7.96;
+//   V-trace bf16 14.78 / 14.43 / 13.88 / 14.00 / 14.29 / 13.62;
+//   Retrace bf16 10.26 / 9.30 / 10.30 / 11.15 / 11.40 / 9.21.
+// Prefetching whole rows before the wait floods L2 when the whole grid is resident at
+// once (one wave: every warp's row requested at the same moment). fp16 inputs move the
+// same bytes as bf16 and take its settings.
+struct PipePrefetch {
+    int first, ahead;
+};
+
+template <Est E, typename TIn, bool MULTI = false>
+constexpr PipePrefetch pipe_prefetch()
+{
+    if (MULTI) return {512, 3};
+    if (std::is_same<TIn, float>::value || E == Est::kGae || E == Est::kTdLambda)
+        return {256, 0};
+    if (E == Est::kReturn) return {1024, 0};
+    return {512, 3};  // V-trace, Retrace
+}
+
+template <Est E, typename TIn, bool MULTI = false>
+void set_pipe_prefetch(Params &p)
+{
+    constexpr PipePrefetch pf = pipe_prefetch<E, TIn, MULTI>();
+    p.pf_first = pf.first;
+    p.pf_ahead = pf.ahead;
+}
+
 // One row per warp, kItems steps per lane, DEPTH chunks' loads in flight ahead of the
 // scan (credit_warp_pipe_kernel). Rows longer than one warp chunk, 16-byte aligned.
-template <Est E, int VEC, bool TRUNC, int DEPTH, typename TIn = float, int MINB = 0>
+// CTAs per SM the register allocator must fit for the pipelined warp rows (0 = no
+// request). One warp per row must be resident at once: 4096 rows need 27 warps per SM on
+// GB300, 7 CTAs of 4 warps, at most 72 registers. fp16 widening costs registers that
+// bf16's shift does not (Retrace: 78-88 against 68-74), so fp16 asks for 7 CTAs per SM.
+template <typename TIn>
+constexpr int pipe_min_blocks()
+{
+    return std::is_same<TIn, __half>::value ? 7 : 0;
+}
+
+template <Est E, int VEC, bool TRUNC, int DEPTH, typename TIn = float,
+          int MINB = pipe_min_blocks<TIn>()>
 cudaError_t launch_warp_pipe(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * kItems;
+    set_pipe_prefetch<E, TIn>(p);
     p.segs = (p.T + CH - 1) / CH;
     p.chunks_per_row = CH / kItems;
     p.rows_per_tile = 1;
@@ -237,10 +291,22 @@ cudaError_t with_vec_trunc(int vec, bool trunc, F &&f)
 // True when a CTA tile holds exactly one row (TILE / 2 < T <= TILE).
 inline bool one_row_per_cta(int T) { return 2 * T > kTile && T <= kTile; }
 
+// Steps per lane of the fp32 warp-owned rows (rows of at most 32 lanes x these steps).
+template <Est E>
+constexpr int warp_rows_items()
+{
+    return kItems;
+}
+
 template <Est E, int VEC, bool TRUNC>
 cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
 {
-    if (path == Path::kWarpRows) return launch_warp_rows<E, VEC, TRUNC>(p, stream);
+    if (path == Path::kWarpRows) {
+        constexpr int I = warp_rows_items<E>();
+        if (I != kItems && p.T <= 32 * I)
+            return launch_warp_rows<E, VEC, TRUNC, float, I>(p, stream);
+        return launch_warp_rows<E, VEC, TRUNC>(p, stream);
+    }
     return launch_cta<E, VEC, TRUNC>(p, path, stream);
 }
 
@@ -254,7 +320,8 @@ void set_beta_pow(Params &p)
     for (int i = 1; i < kItems; ++i) p.beta_pow = beta * p.beta_pow;
 }
 
-// bf16 per-step inputs (uint16_t bit patterns, fp32 arithmetic). Measured on GB300 at
+// 16-bit per-step inputs (TIn: uint16_t bf16 bit patterns or __half; fp32 arithmetic).
+// The two formats move the same bytes and take the same kernels. Measured on GB300 at
 // [4096, 1024], us per launch, the tiles below against a warp per row with its next
 // chunks' loads in flight (credit_warp_pipe_kernel): GAE 14.15 vs 10.84, TD(lambda)
 // 10.64 vs 8.38, V-trace 20.95 vs 14.32, Retrace 15.33 vs 10.24, return 7.86 vs 7.69;
@@ -265,9 +332,10 @@ void set_beta_pow(Params &p)
 // aligned (256-bit stores: GAE 12.77 vs 10.84). Otherwise warp-owned rows up to one
 // warp chunk, CTA tiles (whole rows or the row loop) beyond; GAE rows longer than a warp
 // chunk go to warp-owned rows with 16 steps per lane there.
-template <Est E>
-cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stream)
+template <Est E, typename TIn>
+cudaError_t launch_estimator_narrow(const Params &p_in, int vec, cudaStream_t stream)
 {
+    static_assert(sizeof(TIn) == 2, "16-bit inputs");
     Params p = p_in;
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
@@ -276,22 +344,19 @@ cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stre
         constexpr int D = (E == Est::kVtrace || E == Est::kRetrace) ? 1 : 2;
         constexpr int kFlags64 = kVec16 | kWideLoads;
         if (vec >= 2)
-            return trunc ? launch_warp_pipe<E, kFlags64, true, D, uint16_t>(p, stream)
-                         : launch_warp_pipe<E, kFlags64, false, D, uint16_t>(p, stream);
-        return trunc ? launch_warp_pipe<E, kVec16, true, D, uint16_t>(p, stream)
-                     : launch_warp_pipe<E, kVec16, false, D, uint16_t>(p, stream);
+            return trunc ? launch_warp_pipe<E, kFlags64, true, D, TIn>(p, stream)
+                         : launch_warp_pipe<E, kFlags64, false, D, TIn>(p, stream);
+        return trunc ? launch_warp_pipe<E, kVec16, true, D, TIn>(p, stream)
+                     : launch_warp_pipe<E, kVec16, false, D, TIn>(p, stream);
     }
     // bf16 data loads stay 128-bit; wide flag loads and output stores were measured
     // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout
     // in device memory.
     if (!p.host) vec = vec < 1 ? vec : 1;
     if constexpr (E == Est::kGae) {
-        if (p.T > 32 * kItems) {
-            // 16 steps per lane: beta^16 for the per-lane composite.
-            p.beta_pow = p.gamma_lambda;
-            for (int i = 1; i < 16; ++i) p.beta_pow = p.gamma_lambda * p.beta_pow;
+        if (p.T > 32 * kItems) {  // 16 steps per lane
             return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
-                return launch_warp_rows<E, decltype(v)::value, decltype(r)::value, uint16_t,
+                return launch_warp_rows<E, decltype(v)::value, decltype(r)::value, TIn,
                                         16>(p, stream);
             });
         }
@@ -301,9 +366,18 @@ cudaError_t launch_estimator_bf16(const Params &p_in, int vec, cudaStream_t stre
     return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
         constexpr int V = decltype(v)::value;
         constexpr bool R = decltype(r)::value;
-        if (path == Path::kWarpRows) return launch_warp_rows<E, V, R, uint16_t>(p, stream);
-        return launch_cta<E, V, R, uint16_t>(p, path, stream);
+        if (path == Path::kWarpRows) return launch_warp_rows<E, V, R, TIn>(p, stream);
+        return launch_cta<E, V, R, TIn>(p, path, stream);
     });
+}
+
+// fp32 estimators other than GAE on rows of 513-1024 steps (one row per CTA tile): the
+// pipelined warp rows with this many chunks in flight instead of the CTA tile (0: the
+// CTA tile).
+template <Est E>
+constexpr int fp32_row_pipe_depth()
+{
+    return 0;
 }
 
 // Launch one estimator; `vec` = access level (0 scalar, 1 16-byte aligned rows with
@@ -319,6 +393,12 @@ cudaError_t launch_estimator(const Params &p_in, int vec, cudaStream_t stream)
         if (path == Path::kWarpPipe)
             return trunc ? launch_warp_pipe<E, kVec16, true, 1>(p, stream)
                          : launch_warp_pipe<E, kVec16, false, 1>(p, stream);
+    } else if constexpr (fp32_row_pipe_depth<E>() > 0) {
+        if (path == Path::kCtaRows && one_row_per_cta(p.T) && vec >= 1 && !p.host) {
+            constexpr int D = fp32_row_pipe_depth<E>();
+            return trunc ? launch_warp_pipe<E, kVec16, true, D>(p, stream)
+                         : launch_warp_pipe<E, kVec16, false, D>(p, stream);
+        }
     }
     if ((E == Est::kTdLambda || E == Est::kRetrace) && path == Path::kCtaRows &&
         one_row_per_cta(p.T) && !p.host)
@@ -328,24 +408,65 @@ cudaError_t launch_estimator(const Params &p_in, int vec, cudaStream_t stream)
     });
 }
 
-// One definition per estimator, each in its own translation unit.
-cudaError_t launch_return(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_td_lambda(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_gae(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_vtrace(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_retrace(const Params &p, int vec, cudaStream_t stream);
-// The same with bf16 per-step inputs.
-cudaError_t launch_return_bf16(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_td_lambda_bf16(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_gae_bf16(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_vtrace_bf16(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_retrace_bf16(const Params &p, int vec, cudaStream_t stream);
-// Fused TD(lambda) for p.multi.count lambdas (outputs in p.multi.out).
+// Input formats of the per-step data (rewards, values, ratios, truncation values, x).
+enum class Fmt : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+template <Fmt F>
+struct FmtType;
+template <>
+struct FmtType<Fmt::kF32> {
+    using type = float;
+};
+template <>
+struct FmtType<Fmt::kBF16> {
+    using type = uint16_t;  // bf16 bit patterns
+};
+template <>
+struct FmtType<Fmt::kF16> {
+    using type = __half;
+};
+
+// One estimator in one input format. Each (E, F) pair is instantiated in a translation
+// unit of its own (reverse_unit.cu, compiled once per pair) so the library builds in
+// parallel; the callers see only this declaration.
+template <Est E, Fmt F>
+cudaError_t launch_unit(const Params &p, int vec, cudaStream_t stream);
+
+template <Est E>
+cudaError_t launch_in_format(Fmt f, const Params &p, int vec, cudaStream_t stream)
+{
+    if (f == Fmt::kBF16) return launch_unit<E, Fmt::kBF16>(p, vec, stream);
+    if (f == Fmt::kF16) return launch_unit<E, Fmt::kF16>(p, vec, stream);
+    return launch_unit<E, Fmt::kF32>(p, vec, stream);
+}
+
+// Forward scans in one input format (forward_unit.cu, compiled once per format):
+// p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
+template <Fmt F>
+cudaError_t launch_forward_unit(const Params &p, int vec, cudaStream_t stream);
+
+inline cudaError_t launch_forward_in_format(Fmt f, const Params &p, int vec,
+                                            cudaStream_t stream)
+{
+    if (f == Fmt::kBF16) return launch_forward_unit<Fmt::kBF16>(p, vec, stream);
+    if (f == Fmt::kF16) return launch_forward_unit<Fmt::kF16>(p, vec, stream);
+    return launch_forward_unit<Fmt::kF32>(p, vec, stream);
+}
+
+// Fused calls (fused.cu; fp32 inputs). TD(lambda) for p.multi.count lambdas (outputs in
+// p.multi.out); GAE (parameters and outputs in pg) and V-trace (pv) from one load.
 cudaError_t launch_td_multi(const Params &p, int vec, cudaStream_t stream);
-// Fused GAE (parameters and outputs in pg) and V-trace (pv) from one load of the inputs.
 cudaError_t launch_gae_vtrace(const Params &pg, const Params &pv, int vec, cudaStream_t stream);
-// Forward scans: p.reward = x, p.boot = carried-in values, p.gamma = decay, p.out0 = output.
-cudaError_t launch_forward(const Params &p, int vec, cudaStream_t stream);
-cudaError_t launch_forward_bf16(const Params &p, int vec, cudaStream_t stream);
+
+// GAE with the checks of rlca_gae_ex on a workspace the library owns (ws_bytes at ws);
+// `prepare` runs after every check has passed, right before the launch, and only when
+// the call takes the look-back path (it clears what must start at zero). Returns an
+// RLCA status code.
+int gae_on_library_workspace(const float *reward, const float *value, const uint8_t *terminated,
+                             const uint8_t *truncated, const float *trunc_value,
+                             const float *bootstrap, float gamma, float lambda, int64_t N,
+                             int64_t T, int64_t ld, float *advantages, float *returns,
+                             void *ws, size_t ws_bytes,
+                             cudaError_t (*prepare)(void *ws, cudaStream_t stream), void *stream);
 
 }  // namespace rlca

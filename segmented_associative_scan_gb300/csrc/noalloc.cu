@@ -10,35 +10,55 @@
 #include <mutex>
 
 #include "../../include/rlca.h"
-#include "kernels.cuh"
+#include "launch.cuh"
 
 namespace {
 
 // Fixed scratch: a 256-byte look-back header plus 32 bytes per tile, for at most
-// RLCA_NOALLOC_MAX_TILES tiles (1 MiB + 256 bytes). Zero at module load.
+// RLCA_NOALLOC_MAX_TILES tiles (1 MiB + 256 bytes).
 constexpr size_t kScratchBytes =
     (size_t)rlca::kWsHeaderBytes + (size_t)RLCA_NOALLOC_MAX_TILES * rlca::kTileStateBytes;
 static __device__ __align__(256) unsigned char g_gae_scratch[kScratchBytes];
 
-// Host-side device addresses of g_gae_scratch, one per device, found at set-up.
-constexpr int kMaxDevices = 64;
+// Host-side device addresses of g_gae_scratch, one per device, as last set up.
 std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+void *g_scratch_addr[rlca::kMaxDevices] = {};
 
-// Address of the scratch on the current device, setting it up on first use: the symbol's
-// device address is looked up with that device current and the array is zeroed once.
+// Address of the scratch on the current device. Host code only holds a stand-in for the
+// symbol, so its device address is looked up with the device current, on every call
+// (cheap): after cudaDeviceReset the module is loaded again and the array may move.
+// Whenever the address is new (first use on this device, or the array moved), the whole
+// array is zeroed, synchronously, before it is used.
 void *scratch_on_current_device()
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= rlca::kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gae_scratch) != cudaSuccess || !ptr) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_gae_scratch) != cudaSuccess || !ptr) return nullptr;
-        if (cudaMemset(ptr, 0, kScratchBytes) != cudaSuccess) return nullptr;
+    if (g_scratch_addr[dev] != ptr) {
+        if (cudaMemset(ptr, 0, kScratchBytes) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
         g_scratch_addr[dev] = ptr;
     }
-    return g_scratch_addr[dev];
+    return ptr;
+}
+
+// Runs after every argument check, right before the look-back launch, on its stream.
+// The array keeps the previous call's contents. Tile states carry a launch epoch and
+// need no clearing; the tile and finish counters and the timeout record must start at
+// zero, so clear them (bytes 4..15 of the header; the epoch at byte 0 stays).
+cudaError_t clear_header(void *scratch, cudaStream_t stream)
+{
+    return cudaMemsetAsync(static_cast<unsigned char *>(scratch) + 4, 0, 12, stream);
 }
 
 }  // namespace
@@ -49,19 +69,19 @@ extern "C" int rlca_gae_noalloc(const float *reward, const float *value,
                                 float lambda, int64_t N, int64_t T, int64_t ld,
                                 float *advantages, float *returns, void *stream)
 {
-    const size_t need = rlca_workspace_bytes(N, T);
-    if (need > kScratchBytes) return RLCA_ERR_WORKSPACE;  // more than RLCA_NOALLOC_MAX_TILES
-    if (need == 0)  // rows fit one tile: no scratch involved
+    // Rows that fit one tile, rows numerous enough to fill the GPU one CTA per row, and
+    // every malformed shape go to rlca_gae unchanged: its path uses no workspace, and it
+    // returns its own error codes.
+    if (N <= 0 || T <= rlca::kTile || T > RLCA_MAX_T || ld < T || !rlca::lookback_pays(N))
         return rlca_gae(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
                         lambda, N, T, ld, advantages, returns, stream);
+    // Look-back path: rlca_gae_ex's checks against a workspace of the array's size (more
+    // than RLCA_NOALLOC_MAX_TILES tiles: RLCA_ERR_WORKSPACE), then the header cleared on
+    // the stream and the launch. A call that fails a check enqueues nothing.
     void *scratch = scratch_on_current_device();
     if (!scratch) return RLCA_ERR_LAUNCH;
-    // The array keeps the previous call's contents. Tile states carry a launch epoch and
-    // need no clearing; the tile and finish counters and the timeout record must start
-    // at zero, so clear them (bytes 4..15 of the header; the epoch at byte 0 stays).
-    if (cudaMemsetAsync(static_cast<unsigned char *>(scratch) + 4, 0, 12,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return RLCA_ERR_LAUNCH;
-    return rlca_gae_ex(reward, value, terminated, truncated, trunc_value, bootstrap, gamma,
-                       lambda, N, T, ld, advantages, returns, scratch, kScratchBytes, stream);
+    return rlca::gae_on_library_workspace(reward, value, terminated, truncated, trunc_value,
+                                          bootstrap, gamma, lambda, N, T, ld, advantages,
+                                          returns, scratch, kScratchBytes, clear_header,
+                                          stream);
 }

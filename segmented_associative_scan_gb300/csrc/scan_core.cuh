@@ -15,6 +15,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace rlca {
@@ -102,6 +103,22 @@ __device__ __forceinline__ void st_stream8(float *p, const float *x)
 
 __device__ __forceinline__ uint2 ld_stream(const uint2 *p) { return __ldcs(p); }
 
+// Ask L2 to fetch the 16-byte granules inside [p, p + bytes) of global memory, without
+// waiting and without touching registers or L1 (one bulk prefetch; a hint only). L2 is
+// the point of coherence for global memory, so a later load still sees any write that
+// lands after the prefetch: a kernel may issue it before its grid dependency wait.
+__device__ __forceinline__ void prefetch_l2(const void *p, int64_t bytes)
+{
+    if (bytes > (1 << 24)) bytes = 1 << 24;  // a hint: at most 16 MiB per call
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t lo = (a + 15) & ~(uintptr_t)15;
+    const uintptr_t hi = (a + (uintptr_t)bytes) & ~(uintptr_t)15;
+    if (bytes > 0 && hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo),
+                     "r"((unsigned)(hi - lo))
+                     : "memory");
+}
+
 template <int ITEMS>
 __device__ __forceinline__ constexpr unsigned all_items()
 {
@@ -118,9 +135,11 @@ __device__ __forceinline__ unsigned valid_items(int t0, int T)
 
 // ------------------------------------------------------------- input element types
 
-// Per-step inputs are fp32 or bf16 (`uint16_t` holding the bf16 bit pattern); the
-// arithmetic is fp32 either way. A bf16 value widens to fp32 exactly (its bits are the
-// high half of the fp32 pattern). `kPerVec` elements fill one 128-bit load.
+// Per-step inputs are fp32, bf16 (`uint16_t` holding the bf16 bit pattern) or fp16
+// (`__half`); the arithmetic is fp32 either way. A bf16 value widens to fp32 exactly (its
+// bits are the high half of the fp32 pattern), and so does every fp16 value, subnormals
+// and infinities included (CUDA's half-to-float conversion). `kPerVec` elements fill one
+// 128-bit load.
 template <typename TIn>
 struct InType;
 
@@ -161,6 +180,32 @@ struct InType<uint16_t> {
         for (int i = 0; i < 4; ++i) {
             x[2 * i] = __uint_as_float(w[i] << 16);
             x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+template <>
+struct InType<__half> {
+    static constexpr int kPerVec = 8;
+    __device__ static __forceinline__ float stream(const __half *p)
+    {
+        return __half2float(__ldcs(p));
+    }
+    __device__ static __forceinline__ float cached(const __half *p)
+    {
+        return __half2float(__ldg(p));
+    }
+    __device__ static __forceinline__ void unpack(const uint4 &q, float *x)
+    {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // Word i holds steps 2i (low half) and 2i + 1 (high half).
+            const float2 f = __half22float2(__halves2half2(
+                __ushort_as_half((unsigned short)(w[i] & 0xffffu)),
+                __ushort_as_half((unsigned short)(w[i] >> 16))));
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
         }
     }
 };

@@ -168,3 +168,16 @@ def bf16_rounded(ro):
             setattr(out, k, torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
                     .to(torch.float32).numpy())
     return out
+
+
+def fp16_rounded(ro):
+    """The rollout with every per-step data input rounded to fp16 (round to nearest even,
+    kept as fp32 arrays: fp16 values are exact in fp32)."""
+    import copy
+    out = copy.copy(ro)
+    for k in ("reward", "value", "trunc_value", "log_rho", "q_taken", "expected_q", "rho"):
+        a = getattr(ro, k)
+        if a is not None:
+            setattr(out, k, torch.from_numpy(np.ascontiguousarray(a)).to(torch.float16)
+                    .to(torch.float32).numpy())
+    return out

@@ -1,7 +1,8 @@
-"""The C-ABI library: it builds, loads, exports every symbol include/rlca.h declares,
+"""The C-ABI library: it builds, loads, exports every symbol include/*.h declares,
 and rejects bad arguments on the host with the documented status codes before any
 CUDA call (these tests run without a GPU; the pointers are never dereferenced)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -10,7 +11,7 @@ import pytest
 import segmented_associative_scan_gb300 as rlca
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "rlca.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 OK, NULL, SHAPE, PARAM, ALIAS, WORKSPACE, LAUNCH, TIMEOUT, MEMORY = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
@@ -22,16 +23,18 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rlca_\w+)\s*\(", text)))
+    names = set()
+    for header in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+        names |= set(re.findall(r"\b(rlca_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert "rlca_gae" in names and "rlca_retrace" in names
     for name in names:
-        assert hasattr(lib, name), f"{name} declared in rlca.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
         assert name in rlca.SIGNATURES, f"{name} has no Python binding"
 
 
@@ -168,3 +171,21 @@ def test_gae_vtrace_validation(lib):
     assert f(*gae_vtrace_args(cb=0.0)) == PARAM
     assert f(*gae_vtrace_args(vs=fake(5))) == ALIAS  # vs on advantages
     assert f(*gae_vtrace_args(pg=fake(3))) == ALIAS  # pg on log ratios
+
+
+def test_measure_copy_rejects_bad_arguments(lib):
+    """The measurement entry point validates counts, pointers and alignment on the host."""
+    arr = lambda *p: (ctypes.c_void_p * max(1, len(p)))(*p)
+    ins, fl, outs = arr(fake(1)), arr(fake(2)), arr(fake(3))
+    assert lib.rlca_measure_copy(ins, 0, fl, 1, outs, 1, 1024, 1, None) == PARAM
+    assert lib.rlca_measure_copy(ins, 5, fl, 1, outs, 1, 1024, 1, None) == PARAM
+    assert lib.rlca_measure_copy(ins, 1, fl, 3, outs, 1, 1024, 1, None) == PARAM
+    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 0, 1024, 1, None) == PARAM
+    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, 1024, 3, None) == PARAM
+    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, -1, 1, None) == PARAM
+    assert lib.rlca_measure_copy(arr(None), 1, fl, 1, outs, 1, 1024, 1, None) == NULL
+    assert lib.rlca_measure_copy(arr(fake(1) + 16), 1, fl, 1, outs, 1, 1024, 1,
+                                 None) == WORKSPACE
+    assert lib.rlca_measure_copy(ins, 1, arr(fake(2) + 4), 1, outs, 1, 1024, 1,
+                                 None) == WORKSPACE
+    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, 0, 4, None) == OK

@@ -128,3 +128,31 @@ def test_wide_access_with_ragged_tails(kind, T):
     ro = sr.generic(11, T, seed=T + 17, p_term=0.02, p_trunc=0.01)
     got, ref = run_both(ro, kind, ld=(T + 7) // 8 * 8)
     assert_parity({"o": got}, {"o": ref}, f"{kind} T={T}")
+
+
+@pytest.mark.parametrize("N", [1, 6, 37])
+@pytest.mark.parametrize("T", [260, 264, 500, 512, 520, 768, 1000, 1016, 1024])
+def test_forward_pipelined_rows(N, T):
+    """Rows of 257-1024 steps in 16-byte aligned rows: a warp per row walks its chunks of
+    256 steps from the first with the next chunk's loads in flight; a ragged last chunk is
+    loaded plainly at the end. Episode ends planted on the last step of a chunk (the next
+    chunk starts afresh) and on the first step of one."""
+    ro = sr.generic(N, T, seed=300 + 7 * N + T, p_term=0.01, p_trunc=0.01)
+    for t in (255, 256, 511, 767):
+        if t < T:
+            ro.terminated[0, t] = 1
+            ro.truncated[N - 1, t] = 1 - ro.terminated[N - 1, t]
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind)
+        assert_parity({"o": g}, {"o": r}, f"{kind} N={N} T={T}")
+        g, r = run_both(ro, kind, with_trunc=False, with_init=False)
+        assert_parity({"o": g}, {"o": r}, f"{kind} N={N} T={T} no trunc, no init")
+
+
+@pytest.mark.parametrize("ld_extra,offset", [(4, 0), (8, 0), (0, 4), (12, 8)])
+@pytest.mark.parametrize("T", [264, 1000, 1024])
+def test_forward_pipelined_layouts(T, ld_extra, offset):
+    ro = sr.generic(9, T, seed=400 + T + ld_extra + offset, p_term=0.01, p_trunc=0.01)
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind, ld=T + ld_extra, offset=offset)
+        assert_parity({"o": g}, {"o": r}, f"{kind} T={T} ld+{ld_extra} off={offset}")

@@ -2,10 +2,13 @@
 element, on the same seeded inputs. Tolerance: max|gpu - oracle| <= 1e-4 (1 + max|oracle|)
 per output. Segmentation is checked exactly: a NaN planted in one episode leaves every
 other value bitwise unchanged, and no write lands outside an output's [N, T] block."""
+import copy
+
 import numpy as np
 import pytest
 import torch
 
+import segmented_associative_scan_gb300 as rlca
 import synthetic_rollouts as sr
 from parity_helpers import ESTIMATORS, assert_parity, run_gpu, run_oracle
 
@@ -14,7 +17,6 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module", autouse=True)
 def _device(cuda_device):
-    import segmented_associative_scan_gb300 as rlca
     rlca.build()
     rlca.lib()
     return cuda_device
@@ -146,6 +148,52 @@ def test_importance_ratio_extremes():
         p = dict(lam=lam)
         assert_parity(run_gpu("retrace", ro, p), run_oracle("retrace", ro, p),
                       f"retrace lam={lam}")
+
+
+@pytest.mark.parametrize("T", [300, 1024, 3000])
+def test_retrace_zero_ratio_inside_episodes(T):
+    """rho = +0 is inside Retrace's domain: c_{t+1} = 0 cuts the trace as the formula
+    does (beta_t = +0, not a reset). Planted inside long episodes, at chunk and tile
+    boundaries, then with a NaN later in the episode (0 * NaN is NaN on both sides), and
+    on the look-back path for rows longer than a tile."""
+    ro = sr.generic(4, T, seed=71 + T, p_term=0.0005, p_trunc=0.0)
+    zeros = [t for t in (5, 255, 256, 257, 700, 1023, 1024, 2047, 2048, 2900) if t < T]
+    ro.rho = ro.rho.copy()
+    for i, t in enumerate(zeros):
+        ro.rho[i % 4, t] = 0.0
+        ro.rho[(i + 1) % 4, t] = 0.0
+    assert not np.signbit(ro.rho).any()
+    for lam in (0.95, 1.0):
+        p = dict(lam=lam)
+        assert_parity(run_gpu("retrace", ro, p), run_oracle("retrace", ro, p),
+                      f"retrace rho=+0 lam={lam}")
+    ro.reward = ro.reward.copy()
+    ro.reward[1, min(T - 1, zeros[1] + 10)] = np.nan
+    ro.reward[2, min(T - 1, zeros[-1] + 3)] = np.nan
+    ref = run_oracle("retrace", ro, {})
+    assert np.isnan(ref["q_ret"][1, :zeros[1]]).any()  # the NaN crosses the zero ratio
+    assert_parity(run_gpu("retrace", ro, {}), ref, "retrace rho=+0 with NaN")
+    if T > 1024:
+        ws = rlca.make_workspace(ro.N, T, "cuda")
+        assert_parity(run_gpu("retrace", ro, {}, workspace=ws), ref,
+                      "retrace rho=+0 with NaN, look-back")
+
+
+def test_retrace_negative_ratio_ends_the_trace():
+    """Outside the domain (rho < 0 or -0.0) a ratio is read as the end of the trace: with
+    finite values the result equals the formula with that ratio replaced by +0."""
+    ro = sr.generic(3, 1500, seed=77, p_term=0.001, p_trunc=0.0)
+    neg = ro.rho.copy()
+    neg[0, 100] = -0.0
+    neg[1, 600] = -0.5
+    neg[2, 1024] = -3.0
+    neg[0, 1400] = -0.0
+    clamped = ro.rho.copy()
+    clamped[neg <= 0] = 0.0
+    ro_neg, ro_ref = copy.copy(ro), copy.copy(ro)
+    ro_neg.rho, ro_ref.rho = neg, clamped
+    assert_parity(run_gpu("retrace", ro_neg, {}), run_oracle("retrace", ro_ref, {}),
+                  "retrace negative rho")
 
 
 @pytest.mark.parametrize("ld_extra,offset", [(0, 0), (4, 0), (3, 0), (0, 1), (1, 3), (8, 4)])

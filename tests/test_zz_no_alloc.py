@@ -1,18 +1,20 @@
 """rlca_gae_noalloc: GAE for callers that cannot allocate device memory (a plugin that a
 host framework hands only its input and output buffers, or a loop under a fixed memory
-budget where cudaMalloc could fail or stall the device). For long rows it runs the
-look-back path on a static workspace inside the library.
+budget where cudaMalloc could fail or stall the device). For long rows and few envs it
+runs the look-back path on a static array inside the library; other shapes go to
+rlca_gae unchanged.
 
-Checked through the C ABI against the existing entry point rlca_gae, on two calls in a
-row (the second reuses the static workspace the first one left behind), within the
-tolerance of the other parity tests: max|a - b| <= 1e-4 (1 + max|b|). This file is
-collected last."""
+Checked through the C ABI against the fp64 oracle and against the existing entry point
+rlca_gae, on two calls in a row per shape, with shapes that change between calls (the
+array keeps the previous call's contents), within the tolerance of the other parity
+tests: max|a - b| <= 1e-4 (1 + max|b|). This file is collected last."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import segmented_associative_scan_gb300 as rlca
 import synthetic_rollouts as sr
 
@@ -20,50 +22,108 @@ pytestmark = pytest.mark.gpu
 
 TOL = 1e-4
 MAX_TILES = 32768  # RLCA_NOALLOC_MAX_TILES
+TILE = 1024        # steps per look-back tile
+OK, NULL, SHAPE, PARAM, WORKSPACE = 0, -1, -2, -3, -5
 
 
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _gae_args(ro, dev):
-    d = lambda a: None if a is None else torch.from_numpy(a).to(dev)
-    return [d(ro.reward), d(ro.value), d(ro.terminated), d(ro.truncated),
-            d(ro.trunc_value), d(ro.bootstrap)]
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("N,T", [(64, 5000), (2048, 4096), (300, 1000)])
-def test_noalloc_matches_gae_on_two_calls(cuda_device, N, T):
-    rlca.build()
-    lib = rlca.lib()
-    ro = sr.gae_trunc(N=N, T=T, seed=N + T)
-    g, lam = ro.params["gamma"], ro.params["lam"]
-    inputs = _gae_args(ro, cuda_device)
-    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+def _uses_array(N, T):
+    """True when the call runs the look-back path on the library's array."""
+    return T > TILE and N < 2 * _sms()
 
-    ref_adv = torch.empty((N, T), device=cuda_device)
-    ref_ret = torch.empty_like(ref_adv)
-    assert lib.rlca_gae(*map(_ptr, inputs), g, lam, N, T, T, ref_adv.data_ptr(),
-                        ref_ret.data_ptr(), stream) == 0
-    torch.cuda.synchronize()
-    ref = [ref_adv.cpu().numpy().astype(np.float64), ref_ret.cpu().numpy().astype(np.float64)]
 
-    for call in range(2):
-        adv = torch.full((N, T), float("nan"), device=cuda_device)
-        ret = torch.full((N, T), float("nan"), device=cuda_device)
-        assert lib.rlca_gae_noalloc(*map(_ptr, inputs), g, lam, N, T, T, adv.data_ptr(),
-                                    ret.data_ptr(), stream) == 0
+def _close(got, want, what):
+    got = got.cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - want))
+    assert err <= TOL * (1.0 + np.max(np.abs(want))), f"{what}: max|err| {err:.3e}"
+
+
+class _Case:
+    """One seeded GAE batch on the device, its oracle result and rlca_gae's."""
+
+    def __init__(self, N, T, dev):
+        rlca.build()
+        self.lib = rlca.lib()
+        ro = sr.gae_trunc(N=N, T=T, seed=N + T)
+        self.N, self.T = N, T
+        self.g, self.lam = ro.params["gamma"], ro.params["lam"]
+        d = lambda a: torch.from_numpy(a).to(dev)
+        self.inputs = [d(ro.reward), d(ro.value), d(ro.terminated), d(ro.truncated),
+                       d(ro.trunc_value), d(ro.bootstrap)]
+        self.want = oracle.gae(ro.reward, ro.value, ro.terminated, ro.truncated,
+                               ro.trunc_value, ro.bootstrap, gamma=self.g, lam=self.lam)
+        self.stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        self.dev = dev
+        self.ref = self.run(self.lib.rlca_gae)
+
+    def run(self, fn):
+        adv = torch.full((self.N, self.T), float("nan"), device=self.dev)
+        ret = torch.full((self.N, self.T), float("nan"), device=self.dev)
+        st = fn(*map(_ptr, self.inputs), self.g, self.lam, self.N, self.T, self.T,
+                adv.data_ptr(), ret.data_ptr(), self.stream)
+        assert st == OK, f"status {st}"
         torch.cuda.synchronize()
-        for got, want in zip((adv, ret), ref):
-            got = got.cpu().numpy().astype(np.float64)
-            err = np.max(np.abs(got - want))
-            assert err <= TOL * (1.0 + np.max(np.abs(want))), f"call {call}: {err:.3e}"
+        return adv, ret
+
+    def check_noalloc(self, what):
+        adv, ret = self.run(self.lib.rlca_gae_noalloc)
+        for got, want, ref, name in zip((adv, ret), self.want, self.ref, ("adv", "ret")):
+            _close(got, want, f"{what} {name} vs oracle")
+            _close(got, ref.cpu().numpy().astype(np.float64), f"{what} {name} vs rlca_gae")
 
 
-def test_noalloc_rejects_sizes_beyond_its_static_workspace(cuda_device):
+def test_noalloc_reuses_its_array_across_shapes(cuda_device):
+    """Two calls in a row per shape, the shape changing between pairs: every call here
+    runs look-back on the library's array, which keeps the previous call's state."""
+    shapes = [(64, 5000), (200, 3000), (64, 5000), (5, 70000)]
+    assert all(_uses_array(N, T) for N, T in shapes)
+    cases = {s: _Case(*s, cuda_device) for s in set(shapes)}
+    for k, s in enumerate(shapes):
+        for call in range(2):
+            cases[s].check_noalloc(f"shape {s}, pair {k}, call {call}")
+
+
+def test_noalloc_at_its_exact_tile_limit(cuda_device):
+    """N * ceil(T / 1024) == RLCA_NOALLOC_MAX_TILES fills the array exactly."""
+    N, T = 256, (MAX_TILES // 256) * TILE
+    assert _uses_array(N, T) and N * (T // TILE) == MAX_TILES
+    case = _Case(N, T, cuda_device)
+    case.check_noalloc("limit, call 0")
+    case.check_noalloc("limit, call 1")
+
+
+@pytest.mark.parametrize("N,T", [(16384, 4096), (300, 1000)])
+def test_noalloc_shapes_without_look_back_match_gae(cuda_device, N, T):
+    """Enough rows to fill the GPU (any number of tiles), or rows of one tile: the call
+    is rlca_gae's own, with no workspace, whatever the array's size."""
+    assert not _uses_array(N, T)
+    case = _Case(N, T, cuda_device)
+    case.check_noalloc(f"[{N}, {T}], call 0")
+    case.check_noalloc(f"[{N}, {T}], call 1")
+
+
+def test_noalloc_rejects_look_back_beyond_its_array(cuda_device):
     rlca.build()
     lib = rlca.lib()
-    N, T = MAX_TILES // 4 + 1, 4096  # one tile more than the static workspace holds
-    fake = 1 << 40  # never dereferenced: the size check comes first
-    assert lib.rlca_gae_noalloc(fake, fake + (1 << 36), fake + (2 << 36), None, None, None,
-                                0.99, 0.95, N, T, T, fake + (3 << 36), None, None) == -5
+    fake = 1 << 40  # never dereferenced: every rejection comes before a launch
+    ptrs = lambda: (fake, fake + (1 << 36), fake + (2 << 36), None, None, None)
+    out = fake + (3 << 36)
+    # The most rows that still take look-back, one tile per row more than fits.
+    N = 2 * _sms() - 1
+    T = (MAX_TILES // N + 1) * TILE
+    assert N * (T // TILE) > MAX_TILES
+    assert lib.rlca_gae_noalloc(*ptrs(), 0.99, 0.95, N, T, T, out, None, None) == WORKSPACE
+    # Errors of rlca_gae's checks come first, in its order.
+    assert lib.rlca_gae_noalloc(*ptrs(), 0.99, 0.95, -1, T, T, out, None, None) == SHAPE
+    assert lib.rlca_gae_noalloc(*ptrs(), 0.99, 0.95, N, T, T - 1, out, None, None) == SHAPE
+    assert lib.rlca_gae_noalloc(*ptrs(), float("nan"), 0.95, N, T, T, out, None,
+                                None) == PARAM
+    assert lib.rlca_gae_noalloc(None, *ptrs()[1:], 0.99, 0.95, N, T, T, out, None,
+                                None) == NULL
