@@ -88,7 +88,8 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
     if be in ("trace", "prefix_sum"):
         if T <= 256:
             return "credit_forward_kernel (warp-owned rows, forward)"
-        return ("credit_forward_tile_kernel (whole-row CTA tiles, forward)" if T <= 1024
+        return ("credit_forward_pipe_kernel (a warp per row walking forward, 2 chunks of "
+                "loads in flight)" if T <= 1024
                 else "credit_forward_tile_kernel (CTA row loop, forward)")
     if be == "td_multi":
         if T <= 256:
@@ -120,7 +121,7 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
         return f"credit_scan_kernel<{name}, CTA row loop>"
     if T <= 256:
         return f"credit_warp_kernel<{name}> (warp-owned rows)"
-    if be == "gae":
+    if be == "gae" or (be == "td_lambda" and T > 512):
         return f"credit_warp_pipe_kernel<{name}> (a warp per row, next chunk's loads in flight)"
     return f"credit_scan_kernel<{name}, whole-row CTA tiles>"
 
@@ -128,24 +129,28 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM bytes (read + write) per launch measured by ncu (one captured launch, --set full),
-# keyed by (hash of the kernel sources at the time of the capture, estimator, N, T,
-# workspace); null once the kernels change. Within one captured launch the outputs stay
-# in L2, so these are mostly reads. The committed ncu summaries give the commands.
-_H = "c086cd4238ad4791"
+# Traffic per launch measured by ncu (one captured launch, --set full, the commands in
+# the committed ncu summaries): dram__bytes_read.sum + 32 x
+# lts__t_sectors_srcunit_tex_op_write.sum (within one captured launch the outputs stay
+# in L2, so the DRAM write counter misses them; the L2 write sectors count what the SMs
+# wrote, partial sectors included). Keyed by (hash of the kernel sources at the time of
+# the capture, estimator, N, T, workspace); null once the kernels change.
+_H = "e742cff646344e4b"
 NCU_TRAFFIC = {
-    (_H, "gae", 4096, 1024, False): 44_066_816,
-    (_H, "return", 4096, 1024, False): 20_996_096,
-    (_H, "td_lambda", 4096, 1024, False): 37_788_672,
-    (_H, "vtrace", 4096, 1024, False): 57_277_440,
-    (_H, "retrace", 4096, 1024, False): 73_281_280,
-    (_H, "td_multi", 4096, 1024, False): 39_919_872,
-    (_H, "trace", 4096, 1024, False): 25_190_912,
-    (_H, "gae_bf16", 4096, 1024, False): 26_241_024,
-    (_H, "retrace", 2048, 4096, False): 157_955_328,
-    (_H, "return", 4096, 128, False): 2_650_880,
-    (_H, "return", 16, 524288, True): 43_147_008,
-    (_H, "gae_vtrace", 4096, 1024, False): 67_978_496,
+    (_H, "gae", 4096, 1024, False): 79_473_024,
+    (_H, "return", 4096, 1024, False): 37_774_080,
+    (_H, "td_lambda", 4096, 1024, False): 55_197_312,
+    (_H, "vtrace", 4096, 1024, False): 88_113_920,
+    (_H, "retrace", 4096, 1024, False): 91_365_632,
+    (_H, "td_multi", 4096, 1024, False): 92_548_736,
+    (_H, "gae_vtrace", 4096, 1024, False): 121_675_776,
+    (_H, "trace", 4096, 1024, False): 43_681_920,
+    (_H, "gae_bf16", 4096, 1024, False): 60_775_680,
+    (_H, "gae_fp16", 4096, 1024, False): 64_232_064,
+    (_H, "retrace", 2048, 4096, False): 176_217_344,
+    (_H, "return", 4096, 128, False): 4_750_592,
+    (_H, "vtrace", 8192, 256, False): 44_102_144,
+    (_H, "return", 16, 524288, True): 76_033_824,
 }
 
 
@@ -449,14 +454,20 @@ def warp_walk_chunks(est, T):
     """256-step chunks a warp walks in the kernel the dispatch picks for `est` at T (the
     pipelined warp rows), else 1 (warp-owned rows, CTA tiles)."""
     be = base_est(est)
-    walks = (be == "gae" and 256 < T <= 1024) or (be == "td_multi" and 512 < T <= 1024)
-    return -(-T // 256) if walks and be == est else 1
+    if be != est:  # 16-bit inputs: GAE and the forward scans from 257 steps, the rest 513
+        walks = (256 < T <= 1024 if be in ("gae", "trace", "prefix_sum")
+                 else 512 < T <= 1024)
+    else:
+        walks = ((be in ("gae", "trace", "prefix_sum") and 256 < T <= 1024)
+                 or (be in ("td_multi", "td_lambda") and 512 < T <= 1024))
+    chunks = -(-T // 256) if walks else 1
+    return chunks if chunks in (1, 2, 4) else 1  # the copy takes 1, 2 or 4
 
 
 def time_workload(torch, rlca, device, peak, est, ro, ceiling=True):
     """One estimator alone on the batch `ro` (copies of it rotating past L2 when it is
     large enough): µs per launch, achieved GB/s and the roofline fractions; with
-    `ceiling`, also a plain copy of the same bytes in the same launch shape (fp32 inputs)."""
+    `ceiling`, also the best plain copy of the same bytes (rlca_measure_copy)."""
     params = est_params(est, ro)
     nbytes = algorithmic_bytes(est, ro)
     base = DeviceSet(ro, device, data_dtype_of(torch, est))
@@ -470,12 +481,19 @@ def time_workload(torch, rlca, device, peak, est, ro, ceiling=True):
            "frac_of_8tbs": round(gbs / 8000.0, 4),
            "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1),
            "inputs_exceed_l2": n_sets * nbytes > L2_BYTES}
-    if ceiling and base_est(est) == est:
-        chunks = warp_walk_chunks(est, ro.T)
+    if ceiling:
+        # The best plain copy of the same bytes: in the kernel's launch shape, and for a
+        # kernel that walks rows per warp also in the flat shape (one chunk per warp).
         pats = [copy_pattern(est, x) for x in sets]
-        cu = us_per_step(torch, lambda i: rlca.measure_copy(*pats[i], chunks=chunks), n_sets)
-        out["ceiling_us"] = round(cu, 3)
-        out["frac_of_ceiling"] = round(cu / us, 4)
+        walk = warp_walk_chunks(est, ro.T)
+        shapes = {}
+        for chunks in sorted({1, walk}):
+            shapes[chunks] = us_per_step(
+                torch, lambda i: rlca.measure_copy(*pats[i], chunks=chunks), n_sets)
+        best = min(shapes, key=shapes.get)
+        out["ceiling_us"] = round(shapes[best], 3)
+        out["ceiling_chunks_per_warp"] = best
+        out["frac_of_ceiling"] = round(shapes[best] / us, 4)
     del sets, base
     torch.cuda.empty_cache()
     return out
@@ -828,8 +846,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "traffic_kind": "ncu, one launch: dram__bytes_read.sum + 32 x "
-                            "lts__t_sectors_op_write.sum (bytes written into L2: the outputs "
-                            "stay in L2 until after a captured launch ends)",
+                            "lts__t_sectors_srcunit_tex_op_write.sum (bytes the SMs wrote into "
+                            "L2: the outputs stay in L2 until after a captured launch ends)",
             "kernel": kernel_desc(est, N, T, args.workspace,
                                   torch.cuda.get_device_properties(device).multi_processor_count),
             "algorithmic_bytes_per_launch": round(kernel_bytes_per_step),

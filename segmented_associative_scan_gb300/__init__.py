@@ -56,8 +56,8 @@ SIGNATURES = {
 }
 SIGNATURES["rlca_gae_noalloc"] = SIGNATURES["rlca_gae"]
 # Measurement only (include/rlca_measure.h).
-SIGNATURES["rlca_measure_copy"] = ([_P, ctypes.c_int, _P, ctypes.c_int, _P, ctypes.c_int, _I64,
-                                    ctypes.c_int, _P], ctypes.c_int)
+SIGNATURES["rlca_measure_copy"] = ([_P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int, _P,
+                                    ctypes.c_int, _I64, ctypes.c_int, _P], ctypes.c_int)
 # 16-bit-input variants: the same argument list (the data pointers hold bf16 or fp16).
 for _name in ("rlca_discounted_return", "rlca_td_lambda", "rlca_gae", "rlca_vtrace",
               "rlca_retrace", "rlca_eligibility_trace", "rlca_episodic_prefix_sum"):
@@ -389,12 +389,14 @@ def rlca_episodic_prefix_sum(x, terminated, truncated=None, init=None, sums=None
 
 def measure_copy(inputs, flags, outputs, chunks=1):
     """Measurement only (rlca_measure_copy): one launch that reads every element of the
-    fp32 `inputs` and uint8/bool `flags` and writes every element of the fp32 `outputs`,
-    in the estimator kernels' launch shape (`chunks` 256-element chunks per warp). All
-    tensors are contiguous, on one CUDA device, with the same number of elements."""
+    `inputs` (all float32, or all bfloat16 / float16) and uint8/bool `flags` and writes
+    every element of the fp32 `outputs`, in the estimator kernels' launch shape (`chunks`
+    256-element chunks per warp). All tensors are contiguous, on one CUDA device, with
+    the same number of elements."""
     n = inputs[0].numel()
     dev = inputs[0].device
-    for t, dts in [(t, _F32) for t in list(inputs) + list(outputs)] + \
+    in_dt = _data_dtype(inputs[0])
+    for t, dts in [(t, in_dt) for t in inputs] + [(t, _F32) for t in outputs] + \
             [(t, _FLAG) for t in flags]:
         if not t.is_cuda or t.device != dev or not t.is_contiguous() or t.numel() != n:
             raise ValueError("measure_copy: contiguous tensors of one size on one device")
@@ -402,8 +404,8 @@ def measure_copy(inputs, flags, outputs, chunks=1):
             raise TypeError(f"measure_copy: dtype {t.dtype} not in {dts}")
     arr = lambda ts: (ctypes.c_void_p * max(1, len(ts)))(*[t.data_ptr() for t in ts])
     _check("rlca_measure_copy", lib().rlca_measure_copy(
-        arr(inputs), len(inputs), arr(flags), len(flags), arr(outputs), len(outputs), n,
-        chunks, _stream(dev)))
+        arr(inputs), len(inputs), inputs[0].element_size(), arr(flags), len(flags),
+        arr(outputs), len(outputs), n, chunks, _stream(dev)))
 
 
 # Short names.

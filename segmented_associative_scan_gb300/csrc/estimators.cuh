@@ -64,6 +64,7 @@ struct Params {
     // Geometry of the launch (see kernels.cuh).
     int rows_per_tile;
     int chunks_per_row;
+    int row_shift1;  // log2(chunks_per_row) + 1 when that is a power of two, else 0
     int segs;
     // Decoupled look-back across the tiles of a row (kernels.cuh, Tiling::kLookback).
     void *ws;         // caller-owned workspace: header + one 32-byte state per tile

@@ -103,6 +103,9 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const LaneSlot ls = lane_slot(p, lane);  // index math before the wait: no memory read
+    const int64_t row = job * p.rows_per_tile + ls.local_row;
+    const bool active = ls.local_row < p.rows_per_tile && row < p.N;
     // x and the flags are what the discounted return streams in, too.
     if (p.segs == 1) {
         prefetch_warp_rows<Est::kReturn, TRUNC, TIn>(p, job, p.T);
@@ -112,11 +115,7 @@ __global__ void __launch_bounds__(32 * WARPS) credit_forward_kernel(const Params
     grid_dependency_sync();
     bool last_ended = false;
     if (p.segs == 1) {
-        const int local_row = lane / p.chunks_per_row;
-        const int chunk = lane - local_row * p.chunks_per_row;
-        const int64_t row = job * p.rows_per_tile + local_row;
-        const bool active = local_row < p.rows_per_tile && row < p.N;
-        forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f, false,
+        forward_chunk<ITEMS, VEC, TRUNC, TIn>(p, row, ls.chunk * ITEMS, active, 0.f, false,
                                               &last_ended);
     } else {
         if (job >= p.N) return;  // the whole warp leaves together

@@ -12,11 +12,21 @@ namespace rlca {
 
 // Pipelined forward warp rows: chunks in flight in registers (1 or 2), L2 prefetch
 // before the wait (steps) and ahead of the walk (chunks), and the rows they take
-// (pipe_from < T <= 1024, device memory, 16-byte aligned rows).
+// (pipe_from < T <= 1024, device memory, 16-byte aligned rows). Measured on GB300 at
+// [4096, 1024], eligibility trace / prefix sum, us per launch: CTA tiles with the
+// prefetch 8.19 / 8.40; one chunk in flight, 256 steps before the wait 8.44 / 8.45;
+// two chunks, 256 steps 7.59 / 7.65 (bf16 7.73 / 7.73, fp16 7.66 / 7.67); two chunks,
+// 1024 steps 7.66 / 7.55 (bf16 7.47 / 7.57, fp16 7.87 / 7.89).
 struct ForwardPipe {
     int depth, first, ahead, pipe_from;
 };
-constexpr ForwardPipe kForwardPipe = {1, 256, 0, 256};
+
+template <typename TIn>
+constexpr ForwardPipe forward_pipe()
+{
+    return std::is_same<TIn, uint16_t>::value ? ForwardPipe{2, 1024, 0, 256}
+                                              : ForwardPipe{2, 256, 0, 256};
+}
 
 // Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows up to one CTA
 // tile in device memory with 16-byte aligned rows: a warp per row with its next chunk's
@@ -27,16 +37,17 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
 {
     constexpr int CH = 32 * kItems;
     if constexpr ((VEC & kVec16) != 0) {
-        if (p.T > kForwardPipe.pipe_from && p.T <= kTile && !p.host) {
+        constexpr ForwardPipe fp = forward_pipe<TIn>();
+        if (p.T > fp.pipe_from && p.T <= kTile && !p.host) {
             p.segs = (p.T + CH - 1) / CH;
             p.chunks_per_row = CH / kItems;
             p.rows_per_tile = 1;
-            p.pf_first = kForwardPipe.first;
-            p.pf_ahead = kForwardPipe.ahead;
+            p.pf_first = fp.first;
+            p.pf_ahead = fp.ahead;
             const unsigned grid = (unsigned)((p.N + kWarpsPerCta - 1) / kWarpsPerCta);
-            return launch_pdl(credit_forward_pipe_kernel<kItems, kVec16, TRUNC,
-                                                         kForwardPipe.depth, kWarpsPerCta, TIn>,
-                              grid, 32 * kWarpsPerCta, 0, stream, p);
+            return launch_pdl(
+                credit_forward_pipe_kernel<kItems, kVec16, TRUNC, fp.depth, kWarpsPerCta, TIn>,
+                grid, 32 * kWarpsPerCta, 0, stream, p);
         }
     }
     if (p.T <= CH) {
@@ -44,6 +55,7 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         p.segs = 1;
         p.chunks_per_row = t_pad / kItems;
         p.rows_per_tile = CH / t_pad;
+        set_lane_split(p);
         const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
         const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
         return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta, TIn>, grid,

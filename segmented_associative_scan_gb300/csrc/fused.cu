@@ -22,6 +22,7 @@ cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
         p.chunks_per_row = t_pad / kItems;
         p.rows_per_tile = CH / t_pad;
         p.segs = 1;
+        set_lane_split(p);
         const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
         const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
         return launch_pdl(credit_td_multi_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
@@ -88,6 +89,7 @@ cudaError_t launch_gae_vtrace_variant(Params pg, Params pv, cudaStream_t stream)
         pv.chunks_per_row = t_pad / kItems;
         pv.rows_per_tile = CH / t_pad;
         pv.segs = 1;
+        set_lane_split(pv);
         const int64_t jobs = (pv.N + pv.rows_per_tile - 1) / pv.rows_per_tile;
         grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
         return launch_pdl(credit_gae_vtrace_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta,

@@ -234,6 +234,18 @@ __device__ __forceinline__ void grid_dependency_sync()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Where a lane of a warp that owns whole rows works: its row within the warp's rows and
+// its chunk within that row (a shift when the lanes per row are a power of two).
+struct LaneSlot {
+    int local_row, chunk;
+};
+
+__device__ __forceinline__ LaneSlot lane_slot(const Params &p, int lane)
+{
+    const int r = p.row_shift1 ? lane >> (p.row_shift1 - 1) : lane / p.chunks_per_row;
+    return LaneSlot{r, lane - r * p.chunks_per_row};
+}
+
 // What a CTA of a tile kernel reads first, prefetched into L2 before its grid dependency
 // wait: its whole rows (kRows, kRow) or the first tile it scans (kRowLoop: the row's
 // last tile). One thread per row. Look-back tiles learn their tile only after the wait.
@@ -383,13 +395,12 @@ __global__ void __launch_bounds__(32 * WARPS) credit_td_multi_warp_kernel(const 
     constexpr Est E = Est::kTdLambda;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const LaneSlot ls = lane_slot(p, lane);  // index math before the wait: no memory read
+    const int64_t row = job * p.rows_per_tile + ls.local_row;
+    const bool active = ls.local_row < p.rows_per_tile && row < p.N;
+    const int t0 = ls.chunk * ITEMS;
     prefetch_warp_rows<E, TRUNC, float>(p, job, p.T);
     grid_dependency_sync();
-    const int local_row = lane / p.chunks_per_row;
-    const int chunk = lane - local_row * p.chunks_per_row;
-    const int64_t row = job * p.rows_per_tile + local_row;
-    const bool active = local_row < p.rows_per_tile && row < p.N;
-    const int t0 = chunk * ITEMS;
     Chunk<ITEMS> c;
     load_chunk<E, ITEMS, VEC, TRUNC>(p, row, t0, active, lane, c);
 #pragma unroll
@@ -463,13 +474,12 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_gae_vtrace_warp_kerne
 {
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const LaneSlot ls = lane_slot(pv, lane);
+    const int64_t row = job * pv.rows_per_tile + ls.local_row;
+    const bool active = ls.local_row < pv.rows_per_tile && row < pv.N;
+    const int t0 = ls.chunk * ITEMS;
     prefetch_warp_rows<Est::kVtrace, TRUNC, float>(pv, job, pv.T);
     grid_dependency_sync();
-    const int local_row = lane / pv.chunks_per_row;
-    const int chunk = lane - local_row * pv.chunks_per_row;
-    const int64_t row = job * pv.rows_per_tile + local_row;
-    const bool active = local_row < pv.rows_per_tile && row < pv.N;
-    const int t0 = chunk * ITEMS;
     Chunk<ITEMS> c;
     load_chunk<Est::kVtrace, ITEMS, VEC, TRUNC>(pv, row, t0, active, lane, c);
     {
@@ -546,14 +556,24 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Par
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    // Whole rows per warp: the index math reads no memory, so it can run before the wait
+    // and leave the critical path (measured at [4096, 128]: return 2.22 -> 2.15 us,
+    // TD(lambda) 2.61 -> 2.50). A register-capped kernel does it after the wait (V-trace
+    // at [8192, 256]: 8.22 us after, 8.33 before).
+    LaneSlot ls;
+    int64_t row = 0;
+    bool active = false;
+    auto slot = [&] {
+        ls = lane_slot(p, lane);
+        row = job * p.rows_per_tile + ls.local_row;
+        active = ls.local_row < p.rows_per_tile && row < p.N;
+    };
+    if constexpr (MINB == 0) slot();
     prefetch_warp_rows<E, TRUNC, TIn>(p, job, 1024);
     grid_dependency_sync();
     if (p.segs == 1) {
-        const int local_row = lane / p.chunks_per_row;
-        const int chunk = lane - local_row * p.chunks_per_row;
-        const int64_t row = job * p.rows_per_tile + local_row;
-        const bool active = local_row < p.rows_per_tile && row < p.N;
-        warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, chunk * ITEMS, active, 0.f);
+        if constexpr (MINB != 0) slot();
+        warp_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, ls.chunk * ITEMS, active, 0.f);
     } else {
         if (job >= p.N) return;  // the whole warp leaves together
         float carry = 0.f;

@@ -55,6 +55,15 @@ cudaError_t launch_pdl(Kernel kernel, unsigned grid, unsigned block, size_t smem
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Warp-owned whole rows: lanes per row as a shift when a power of two (lane_slot).
+inline void set_lane_split(Params &p)
+{
+    const int c = p.chunks_per_row;
+    int k = 0;
+    while ((1 << k) < c) ++k;
+    p.row_shift1 = (c > 0 && (1 << k) == c) ? k + 1 : 0;
+}
+
 // ------------------------------------------------------------------ kernel choice
 
 enum class Path : int { kCtaRows, kCtaRowLoop, kLookback, kWarpRows, kWarpPipe };
@@ -177,6 +186,7 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
         p.segs = 1;
         p.chunks_per_row = t_pad / ITEMS;
         p.rows_per_tile = CH / t_pad;
+        set_lane_split(p);
         jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
     } else {
         p.segs = (p.T + CH - 1) / CH;
@@ -213,8 +223,9 @@ template <Est E, typename TIn, bool MULTI = false>
 constexpr PipePrefetch pipe_prefetch()
 {
     if (MULTI) return {512, 3};
-    if (std::is_same<TIn, float>::value || E == Est::kGae || E == Est::kTdLambda)
-        return {256, 0};
+    if (std::is_same<TIn, float>::value) return E == Est::kTdLambda ? PipePrefetch{512, 3}
+                                                                    : PipePrefetch{256, 0};
+    if (E == Est::kGae || E == Est::kTdLambda) return {256, 0};
     if (E == Est::kReturn) return {1024, 0};
     return {512, 3};  // V-trace, Retrace
 }
@@ -266,10 +277,12 @@ cudaError_t launch_warp_pipe(Params p, cudaStream_t stream)
 //   row loop [2048, 4096]: return 15.79 vs 15.43, TD 19.90 vs 19.10, V-trace 32.46 vs
 //     31.38, Retrace 30.77 vs 27.63, GAE 24.86 vs 23.51, fused TD 33.82 vs 32.45;
 //   one row per CTA [4096, 1024]: return 7.71 vs 7.52, GAE 12.52 vs 12.05, V-trace 16.88
-//     vs 16.70, fused TD 17.33 vs 17.11, but TD 10.07 vs 10.16, Retrace 15.22 vs 15.36
-//     and the forward scan 8.46 vs 8.53, which keep 128-bit access there;
+//     vs 16.70, fused TD 17.33 vs 17.11, but TD 10.07 vs 10.16 and the forward scan 8.46
+//     vs 8.53, which keep 128-bit access there (Retrace was 15.22 vs 15.36 before the
+//     L2 prefetch, 14.42 vs 14.16 with it: 256-bit now);
 //   pipelined warp rows, GAE [4096, 1024]: 12.90 with 128-bit access, 13.24 with
-//     256-bit, 13.27 with 256-bit loads and 128-bit stores: 128-bit there.
+//     256-bit, 13.27 with 256-bit loads and 128-bit stores: 128-bit there (with the L2
+//     prefetch 12.30 vs 12.78 with 256-bit stores).
 // Wide loads alone or wide stores alone were slower than either.
 constexpr int kWideVec = kVec16 | kWideLoads | kWideStores;
 
@@ -373,11 +386,15 @@ cudaError_t launch_estimator_narrow(const Params &p_in, int vec, cudaStream_t st
 
 // fp32 estimators other than GAE on rows of 513-1024 steps (one row per CTA tile): the
 // pipelined warp rows with this many chunks in flight instead of the CTA tile (0: the
-// CTA tile).
+// CTA tile). Measured on GB300 at [4096, 1024] with the L2 prefetch, us per launch, CTA
+// tile / one chunk in flight (256 steps before the wait) / two chunks / one chunk
+// (512 steps before the wait, 3 chunks ahead): return 6.84 / 7.82 / 7.78 / 7.43;
+// TD(lambda) 10.14 / 9.52 / 11.93 / 9.34; V-trace 14.88 / 16.80 / 16.80 / 16.87;
+// Retrace 14.48 / 15.53 / 15.56 / 16.69.
 template <Est E>
 constexpr int fp32_row_pipe_depth()
 {
-    return 0;
+    return E == Est::kTdLambda ? 1 : 0;
 }
 
 // Launch one estimator; `vec` = access level (0 scalar, 1 16-byte aligned rows with
@@ -400,8 +417,11 @@ cudaError_t launch_estimator(const Params &p_in, int vec, cudaStream_t stream)
                          : launch_warp_pipe<E, kVec16, false, D>(p, stream);
         }
     }
-    if ((E == Est::kTdLambda || E == Est::kRetrace) && path == Path::kCtaRows &&
-        one_row_per_cta(p.T) && !p.host)
+    // TD(lambda) keeps 128-bit access on a CTA row (measured 10.07 vs 10.16 us at
+    // [4096, 1024]); it takes the CTA row only without 16-byte aligned rows now.
+    // Retrace moved to 256-bit with the L2 prefetch: 14.16 vs 14.42 us, and every output
+    // sector written whole (1.19x the output bytes reached L2 with 128-bit stores).
+    if (E == Est::kTdLambda && path == Path::kCtaRows && one_row_per_cta(p.T) && !p.host)
         vec = vec < 1 ? vec : 1;
     return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
         return launch_path<E, decltype(v)::value, decltype(r)::value>(p, path, stream);

@@ -177,15 +177,17 @@ def test_measure_copy_rejects_bad_arguments(lib):
     """The measurement entry point validates counts, pointers and alignment on the host."""
     arr = lambda *p: (ctypes.c_void_p * max(1, len(p)))(*p)
     ins, fl, outs = arr(fake(1)), arr(fake(2)), arr(fake(3))
-    assert lib.rlca_measure_copy(ins, 0, fl, 1, outs, 1, 1024, 1, None) == PARAM
-    assert lib.rlca_measure_copy(ins, 5, fl, 1, outs, 1, 1024, 1, None) == PARAM
-    assert lib.rlca_measure_copy(ins, 1, fl, 3, outs, 1, 1024, 1, None) == PARAM
-    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 0, 1024, 1, None) == PARAM
-    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, 1024, 3, None) == PARAM
-    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, -1, 1, None) == PARAM
-    assert lib.rlca_measure_copy(arr(None), 1, fl, 1, outs, 1, 1024, 1, None) == NULL
-    assert lib.rlca_measure_copy(arr(fake(1) + 16), 1, fl, 1, outs, 1, 1024, 1,
-                                 None) == WORKSPACE
-    assert lib.rlca_measure_copy(ins, 1, arr(fake(2) + 4), 1, outs, 1, 1024, 1,
-                                 None) == WORKSPACE
-    assert lib.rlca_measure_copy(ins, 1, fl, 1, outs, 1, 0, 4, None) == OK
+    call = lambda i=ins, ni=1, eb=4, f=fl, nf=1, o=outs, no=1, n=1024, c=1: \
+        lib.rlca_measure_copy(i, ni, eb, f, nf, o, no, n, c, None)
+    assert call(ni=0) == PARAM
+    assert call(ni=5) == PARAM
+    assert call(nf=3) == PARAM
+    assert call(no=0) == PARAM
+    assert call(c=3) == PARAM
+    assert call(n=-1) == PARAM
+    assert call(eb=8) == PARAM
+    assert call(i=arr(None)) == NULL
+    assert call(i=arr(fake(1) + 16)) == WORKSPACE      # fp32 inputs: 32-byte aligned
+    assert call(i=arr(fake(1) + 8), eb=2) == WORKSPACE
+    assert call(f=arr(fake(2) + 4)) == WORKSPACE
+    assert call(n=0, c=4) == OK
