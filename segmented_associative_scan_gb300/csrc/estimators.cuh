@@ -355,9 +355,11 @@ __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chun
             const float rho = expf(c.x[j]);
             c.x[j] = rho;
             const float rho_hat = rho < p.rho_bar ? rho : p.rho_bar;
-            const float cc = p.lambda * (rho < p.c_bar ? rho : p.c_bar);
+            const float cmin = rho < p.c_bar ? rho : p.c_bar;
             const float nxt = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j);
-            e[j] = Affine{rho_hat * (fmaf(p.gamma, nxt, r) - c.v[j]), stop ? kResetB : p.gamma * cc};
+            const float delta = fmaf(p.gamma, nxt, r) - c.v[j];
+            c.sv[j] = delta;  // the policy-gradient target reuses the TD error
+            e[j] = Affine{rho_hat * delta, stop ? kResetB : p.gamma_lambda * cmin};
         } else {  // Retrace: beta_t uses the trace of step t+1
             const float rho1 = at_or_next(c.y, c.y_next, j);
             const float c1 = p.lambda * (rho1 < 1.f ? rho1 : 1.f);
@@ -433,13 +435,15 @@ __device__ __forceinline__ void epilogue(const Params &p, const Chunk<ITEMS> &c,
             o0[j] = A[j];
             o1[j] = A[j] + c.v[j];
         } else if (E == Est::kVtrace) {
+            // pg_t = rho_pg (r_t + gamma vs_{t+1} - V_t) = rho_pg (delta_t + gamma A_{t+1})
+            // inside an episode (vs_{t+1} = V_{t+1} + A_{t+1}), rho_pg delta_t at its last
+            // step (the successor value already in delta_t); build() left delta_t in sv.
             const bool stop = (c.stop >> j) & 1u;
             const float rho = c.x[j];
             const float a_next = (j + 1 < ITEMS) ? A[j + 1] : a_after;
-            const float q = stop ? c.sv[j] : at_or_next(c.v, c.v_next, j) + a_next;
             const float rho_pg = rho < p.pg_rho_bar ? rho : p.pg_rho_bar;
             o0[j] = c.v[j] + A[j];
-            o1[j] = rho_pg * (fmaf(p.gamma, q, c.r[j]) - c.v[j]);
+            o1[j] = rho_pg * (stop ? c.sv[j] : fmaf(p.gamma, a_next, c.sv[j]));
         } else {
             o0[j] = A[j] + c.v[j];
         }
