@@ -106,7 +106,7 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
     if narrow:
         if T <= 256:
             return f"credit_warp_kernel<{name}> (warp-owned rows, 8 steps/lane)"
-        pipe_from = 256 if be == "gae" else 512
+        pipe_from = 256 if be == "gae" else (1024 if be == "return" else 512)
         depth = 1 if be in ("vtrace", "retrace") else 2
         if pipe_from < T <= 1024:
             return (f"credit_warp_pipe_kernel<{name}> (a warp per row, {depth} chunk(s) of "
@@ -135,22 +135,24 @@ L2_BYTES = 129 * 2 ** 20
 # in L2, so the DRAM write counter misses them; the L2 write sectors count what the SMs
 # wrote, partial sectors included). Keyed by (hash of the kernel sources at the time of
 # the capture, estimator, N, T, workspace); null once the kernels change.
-_H = "e742cff646344e4b"
+_H = "8203e77064a7f7ce"
 NCU_TRAFFIC = {
-    (_H, "gae", 4096, 1024, False): 79_473_024,
+    (_H, "gae", 4096, 1024, False): 79_198_976,
     (_H, "return", 4096, 1024, False): 37_774_080,
-    (_H, "td_lambda", 4096, 1024, False): 55_197_312,
-    (_H, "vtrace", 4096, 1024, False): 88_113_920,
-    (_H, "retrace", 4096, 1024, False): 91_365_632,
-    (_H, "td_multi", 4096, 1024, False): 92_548_736,
-    (_H, "gae_vtrace", 4096, 1024, False): 121_675_776,
-    (_H, "trace", 4096, 1024, False): 43_681_920,
-    (_H, "gae_bf16", 4096, 1024, False): 60_775_680,
-    (_H, "gae_fp16", 4096, 1024, False): 64_232_064,
-    (_H, "retrace", 2048, 4096, False): 176_217_344,
+    (_H, "td_lambda", 4096, 1024, False): 55_095_680,
+    (_H, "vtrace", 4096, 1024, False): 88_113_664,
+    (_H, "retrace", 4096, 1024, False): 88_111_872,
+    (_H, "td_multi", 4096, 1024, False): 92_505_344,
+    (_H, "gae_vtrace", 4096, 1024, False): 121_681_408,
+    (_H, "trace", 4096, 1024, False): 43_529_856,
+    (_H, "gae_bf16", 4096, 1024, False): 60_959_360,
+    (_H, "gae_fp16", 4096, 1024, False): 64_237_056,
+    (_H, "return_bf16", 4096, 1024, False): 29_385_472,
+    (_H, "vtrace_fp16", 4096, 1024, False): 75_026_816,
+    (_H, "retrace", 2048, 4096, False): 176_217_600,
     (_H, "return", 4096, 128, False): 4_750_592,
-    (_H, "vtrace", 8192, 256, False): 44_102_144,
-    (_H, "return", 16, 524288, True): 76_033_824,
+    (_H, "vtrace", 8192, 256, False): 44_100_608,
+    (_H, "return", 16, 524288, True): 76_034_336,
 }
 
 
@@ -454,9 +456,9 @@ def warp_walk_chunks(est, T):
     """256-step chunks a warp walks in the kernel the dispatch picks for `est` at T (the
     pipelined warp rows), else 1 (warp-owned rows, CTA tiles)."""
     be = base_est(est)
-    if be != est:  # 16-bit inputs: GAE and the forward scans from 257 steps, the rest 513
-        walks = (256 < T <= 1024 if be in ("gae", "trace", "prefix_sum")
-                 else 512 < T <= 1024)
+    if be != est:  # 16-bit inputs: GAE and the forward scans from 257 steps, the rest
+        walks = (256 < T <= 1024 if be in ("gae", "trace", "prefix_sum")  # from 513, but
+                 else be != "return" and 512 < T <= 1024)               # not the return
     else:
         walks = ((be in ("gae", "trace", "prefix_sum") and 256 < T <= 1024)
                  or (be in ("td_multi", "td_lambda") and 512 < T <= 1024))

@@ -139,7 +139,7 @@ template <int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4, typename TIn
           int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_forward_pipe_kernel(const Params p)
 {
-    static_assert(DEPTH == 1 || DEPTH == 2, "one or two chunks in flight");
+    static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three chunks in flight");
     static_assert(VEC & kVec16, "raw chunks are read with vector loads");
     constexpr Est E = Est::kReturn;  // streams x (as reward) and the flags, nothing else
     constexpr int CH = 32 * ITEMS;
@@ -152,9 +152,11 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_forward_pipe_kernel(c
     const int full = p.T / CH;
     float carry = 0.f;
     bool ended_before = false;
-    RawChunk<E, ITEMS, TIn> w0, w1;
-    if (full > 0) load_raw<E, ITEMS, VEC, TRUNC>(p, off, lane * ITEMS, lane, w0);
-    if (DEPTH == 2 && full > 1) load_raw<E, ITEMS, VEC, TRUNC>(p, off, CH + lane * ITEMS, lane, w1);
+    // w[d] holds chunk s + d (registers: every index below is a compile-time constant).
+    RawChunk<E, ITEMS, TIn> w[DEPTH];
+#pragma unroll
+    for (int d = 0; d < DEPTH; ++d)
+        if (d < full) load_raw<E, ITEMS, VEC, TRUNC>(p, off, d * CH + lane * ITEMS, lane, w[d]);
     for (int s = 0; s < full; ++s) {
         const int t0 = s * CH + lane * ITEMS;
         if (lane == 0 && p.pf_ahead > 0 && (s + p.pf_ahead) * CH < p.T) {
@@ -162,18 +164,17 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_forward_pipe_kernel(c
             prefetch_row<E, TRUNC, TIn>(p, row, lo, lo + CH < p.T ? lo + CH : p.T);
         }
         float x[ITEMS];
-        widen_words<TIn>(w0.r, x);
+        widen_words<TIn>(w[0].r, x);
         unsigned ended = 0;
 #pragma unroll
         for (int k = 0; k < ITEMS / 4; ++k)
-            ended |= nonzero_bytes(TRUNC ? (w0.term[k] | w0.trunc[k]) : w0.term[k]) << (4 * k);
-        if (DEPTH == 2) {
-            w0 = w1;
-            if (s + 2 < full)
-                load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s + 2) * CH + lane * ITEMS, lane, w1);
-        } else if (s + 1 < full) {
-            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s + 1) * CH + lane * ITEMS, lane, w0);
-        }
+            ended |= nonzero_bytes(TRUNC ? (w[0].term[k] | w[0].trunc[k]) : w[0].term[k])
+                     << (4 * k);
+#pragma unroll
+        for (int d = 0; d + 1 < DEPTH; ++d) w[d] = w[d + 1];
+        if (s + DEPTH < full)
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s + DEPTH) * CH + lane * ITEMS, lane,
+                                           w[DEPTH - 1]);
         carry = forward_chunk_scan<ITEMS, VEC, TIn>(p, row, t0, true, x, ended,
                                                     all_items<ITEMS>(), carry, ended_before,
                                                     &ended_before);

@@ -16,7 +16,9 @@ namespace rlca {
 // [4096, 1024], eligibility trace / prefix sum, us per launch: CTA tiles with the
 // prefetch 8.19 / 8.40; one chunk in flight, 256 steps before the wait 8.44 / 8.45;
 // two chunks, 256 steps 7.59 / 7.65 (bf16 7.73 / 7.73, fp16 7.66 / 7.67); two chunks,
-// 1024 steps 7.66 / 7.55 (bf16 7.47 / 7.57, fp16 7.87 / 7.89).
+// 1024 steps 7.66 / 7.55 (bf16 7.47 / 7.57, fp16 7.87 / 7.89); three chunks (fp32 1024
+// steps, bf16 1024, fp16 256): fp32 8.08 / 8.07, bf16 7.06 / 7.07 against 7.29 / 7.29
+// with two, fp16 7.36 / 7.36 against 7.61 / 7.62 (fp32 58-64 registers, one wave still).
 struct ForwardPipe {
     int depth, first, ahead, pipe_from;
 };
@@ -24,8 +26,9 @@ struct ForwardPipe {
 template <typename TIn>
 constexpr ForwardPipe forward_pipe()
 {
-    return std::is_same<TIn, uint16_t>::value ? ForwardPipe{2, 1024, 0, 256}
-                                              : ForwardPipe{2, 256, 0, 256};
+    if (std::is_same<TIn, uint16_t>::value) return {3, 1024, 0, 256};  // bf16
+    if (std::is_same<TIn, __half>::value) return {3, 256, 0, 256};
+    return {2, 256, 0, 256};
 }
 
 // Rows of at most one warp chunk (256 steps): warp-owned rows. Longer rows up to one CTA
@@ -57,9 +60,9 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
         p.rows_per_tile = CH / t_pad;
         set_lane_split(p);
         const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
-        const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-        return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpsPerCta, TIn>, grid,
-                          32 * kWarpsPerCta, 0, stream, p);
+        const unsigned grid = (unsigned)((jobs + kWarpRowsPerCta - 1) / kWarpRowsPerCta);
+        return launch_pdl(credit_forward_kernel<kItems, VEC, TRUNC, kWarpRowsPerCta, TIn>,
+                          grid, 32 * kWarpRowsPerCta, 0, stream, p);
     }
     if (p.T <= kTile) {
         const int t_pad = (p.T + kItems - 1) / kItems * kItems;

@@ -24,9 +24,9 @@ cudaError_t launch_td_multi_variant(Params p, cudaStream_t stream)
         p.segs = 1;
         set_lane_split(p);
         const int64_t jobs = (p.N + p.rows_per_tile - 1) / p.rows_per_tile;
-        const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-        return launch_pdl(credit_td_multi_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta>, grid,
-                          32 * kWarpsPerCta, 0, stream, p);
+        const unsigned grid = (unsigned)((jobs + kWarpRowsPerCta - 1) / kWarpRowsPerCta);
+        return launch_pdl(credit_td_multi_warp_kernel<kItems, VEC, TRUNC, kWarpRowsPerCta>,
+                          grid, 32 * kWarpRowsPerCta, 0, stream, p);
     }
     if constexpr ((VEC & kVec16) != 0) {
         if (2 * p.T > kTile && p.T <= kTile && !p.host) {
@@ -91,10 +91,10 @@ cudaError_t launch_gae_vtrace_variant(Params pg, Params pv, cudaStream_t stream)
         pv.segs = 1;
         set_lane_split(pv);
         const int64_t jobs = (pv.N + pv.rows_per_tile - 1) / pv.rows_per_tile;
-        grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-        return launch_pdl(credit_gae_vtrace_warp_kernel<kItems, VEC, TRUNC, kWarpsPerCta,
-                                                        kPairMinBlocks>,
-                          grid, 32 * kWarpsPerCta, 0, stream, pg, pv);
+        grid = (unsigned)((jobs + kWarpRowsPerCta - 1) / kWarpRowsPerCta);
+        return launch_pdl(credit_gae_vtrace_warp_kernel<kItems, VEC, TRUNC, kWarpRowsPerCta,
+                                                        kPairMinBlocks * 4 / kWarpRowsPerCta>,
+                          grid, 32 * kWarpRowsPerCta, 0, stream, pg, pv);
     }
     if (pv.T <= kTile) {
         const int t_pad = (pv.T + kItems - 1) / kItems * kItems;

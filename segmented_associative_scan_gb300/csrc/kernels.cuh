@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Par
 template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, typename TIn, typename Scan>
 __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan &&scan)
 {
-    static_assert(DEPTH == 1 || DEPTH == 2, "one or two chunks in flight");
+    static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three chunks in flight");
     static_assert(VEC & kVec16, "raw chunks are read with vector loads");
     constexpr int CH = 32 * ITEMS;
     const int lane = threadIdx.x & 31;
@@ -606,24 +606,24 @@ __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan
         --s;
     }
     if (s < 0) return;
-    RawChunk<E, ITEMS, TIn> w0, w1;
-    load_raw<E, ITEMS, VEC, TRUNC>(p, off, s * CH + lane * ITEMS, lane, w0);
-    if (DEPTH == 2 && s >= 1)
-        load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w1);
+    // w[d] holds chunk s - d (registers: every index below is a compile-time constant).
+    RawChunk<E, ITEMS, TIn> w[DEPTH];
+#pragma unroll
+    for (int d = 0; d < DEPTH; ++d)
+        if (s - d >= 0)
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - d) * CH + lane * ITEMS, lane, w[d]);
     for (; s >= 0; --s) {
         const int t0 = s * CH + lane * ITEMS;
         if (lane == 0 && p.pf_ahead > 0 && s >= p.pf_ahead)  // beyond the registers' reach
             prefetch_row<E, TRUNC, TIn>(p, row, (s - p.pf_ahead) * CH,
                                         (s - p.pf_ahead + 1) * CH);
         Chunk<ITEMS> c;
-        unpack_raw<E, ITEMS, TRUNC>(w0, p.T, t0, lane, c);
-        if (DEPTH == 2) {
-            w0 = w1;
-            if (s >= 2)
-                load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 2) * CH + lane * ITEMS, lane, w1);
-        } else if (s >= 1) {
-            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - 1) * CH + lane * ITEMS, lane, w0);
-        }
+        unpack_raw<E, ITEMS, TRUNC>(w[0], p.T, t0, lane, c);
+#pragma unroll
+        for (int d = 0; d + 1 < DEPTH; ++d) w[d] = w[d + 1];
+        if (s - DEPTH >= 0)
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - DEPTH) * CH + lane * ITEMS, lane,
+                                           w[DEPTH - 1]);
         scan(t0, c);
     }
 }

@@ -18,8 +18,13 @@ namespace rlca {
 constexpr int kThreads = 128;
 constexpr int kItems = 8;
 constexpr int kTile = kThreads * kItems;
-// Warp-owned rows: 4 independent warps per CTA, 32 lanes x 8 steps per chunk.
+// Warp-owned rows: independent warps per CTA, 32 lanes x 8 steps per chunk; 4 for the
+// pipelined rows, kWarpRowsPerCta for the rows a warp owns whole (short rows). Measured
+// on GB300, 2 / 4 / 8 warps per CTA, us per launch: TD(lambda) [4096, 128] 2.375 / 2.50 /
+// 2.63, fused TD(lambda) 3.31 / 3.36 / 3.50, return 2.154 / 2.156 / 2.252, V-trace
+// [8192, 256] 8.13 / 8.15 / 9.23.
 constexpr int kWarpsPerCta = 4;
+constexpr int kWarpRowsPerCta = 2;
 
 // Look-back tiles of an [N, T] problem (0 when T fits one tile: no look-back needed).
 inline int64_t lookback_tiles(int64_t N, int64_t T)
@@ -163,12 +168,15 @@ cudaError_t launch_cta(Params p, Path path, cudaStream_t stream)
 // ------------------------------------------------------------------ warp paths
 
 // CTAs per SM the warp-owned-rows kernel asks the register allocator to fit (0 = no
-// request). V-trace's needs 80 registers (6 CTAs per SM); capped at 7 per SM (72
-// registers, 28 bytes of spill) it ran faster on [8192, 256]: 9.16 us against 9.72.
+// request). V-trace's needs 80 registers (6 CTAs of 4 warps per SM); capped at 28 warps
+// per SM (72 registers, 28 bytes of spill) it ran faster on [8192, 256]: 9.16 us
+// against 9.72.
 template <Est E, typename TIn, int ITEMS>
 constexpr int warp_min_blocks()
 {
-    return (E == Est::kVtrace && std::is_same<TIn, float>::value && ITEMS == kItems) ? 7 : 0;
+    return (E == Est::kVtrace && std::is_same<TIn, float>::value && ITEMS == kItems)
+               ? 28 / kWarpRowsPerCta
+               : 0;
 }
 
 template <Est E, int VEC, bool TRUNC, typename TIn = float, int ITEMS = kItems>
@@ -194,10 +202,10 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
         p.rows_per_tile = 1;
         jobs = p.N;
     }
-    const unsigned grid = (unsigned)((jobs + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(credit_warp_kernel<E, ITEMS, VEC, TRUNC, kWarpsPerCta, TIn,
+    const unsigned grid = (unsigned)((jobs + kWarpRowsPerCta - 1) / kWarpRowsPerCta);
+    return launch_pdl(credit_warp_kernel<E, ITEMS, VEC, TRUNC, kWarpRowsPerCta, TIn,
                                          warp_min_blocks<E, TIn, ITEMS>()>,
-                      grid, 32 * kWarpsPerCta, 0, stream, p);
+                      grid, 32 * kWarpRowsPerCta, 0, stream, p);
 }
 
 // L2 prefetch of the pipelined warp rows: steps prefetched before the grid dependency
@@ -352,7 +360,11 @@ cudaError_t launch_estimator_narrow(const Params &p_in, int vec, cudaStream_t st
     Params p = p_in;
     set_beta_pow<E>(p);
     const bool trunc = p.trunc != nullptr;
-    const int pipe_from = E == Est::kGae ? 32 * kItems : 64 * kItems;
+    // The 16-bit discounted return keeps CTA rows up to one tile: with the L2 prefetch
+    // and 256-bit output stores they beat its pipelined warp rows at [4096, 1024] (bf16
+    // 6.48 vs 7.08 us, fp16 6.45 vs 6.89); the other estimators lost there (TD(lambda)
+    // 9.52 vs 7.86, GAE 14.0 vs 10.9, V-trace 15.2 vs 13.9, Retrace 12.6 vs 9.2, bf16).
+    const int pipe_from = E == Est::kGae ? 32 * kItems : (E == Est::kReturn ? kTile : 64 * kItems);
     if (!p.host && vec >= 1 && p.T > pipe_from && p.T <= kTile) {
         constexpr int D = (E == Est::kVtrace || E == Est::kRetrace) ? 1 : 2;
         constexpr int kFlags64 = kVec16 | kWideLoads;
@@ -362,10 +374,10 @@ cudaError_t launch_estimator_narrow(const Params &p_in, int vec, cudaStream_t st
         return trunc ? launch_warp_pipe<E, kVec16, true, D, TIn>(p, stream)
                      : launch_warp_pipe<E, kVec16, false, D, TIn>(p, stream);
     }
-    // bf16 data loads stay 128-bit; wide flag loads and output stores were measured
-    // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout
-    // in device memory.
-    if (!p.host) vec = vec < 1 ? vec : 1;
+    // 16-bit data loads stay 128-bit; wide flag loads and output stores were measured
+    // slower for bf16 GAE at [4096, 1024] (14.63 vs 14.25 us), so 128-bit throughout in
+    // device memory, except the return's CTA rows (6.48 vs 6.74 us, bf16).
+    if (!p.host && !(E == Est::kReturn && p.T > 32 * kItems)) vec = vec < 1 ? vec : 1;
     if constexpr (E == Est::kGae) {
         if (p.T > 32 * kItems) {  // 16 steps per lane
             return with_vec_trunc(vec, trunc, [&](auto v, auto r) {
