@@ -218,7 +218,8 @@ cudaError_t launch_warp_rows(Params p, cudaStream_t stream)
 //   fused TD(lambda), 3 lambdas, 15.63 / 14.82 / 15.08 / 16.49 / 15.72 / 14.39;
 //   return bf16 7.79 / 7.50 / 8.28 / 7.10 / 8.49 / 7.35;
 //   TD(lambda) bf16 8.58 / 7.76 / 9.04 / 8.15 / 8.98 / 7.96;
-//   V-trace bf16 14.78 / 14.43 / 13.88 / 14.00 / 14.29 / 13.62;
+//   V-trace bf16 14.78 / 14.43 / 13.88 / 14.00 / 14.29 / 13.62 (two waves of warps then,
+//     at 87-90 registers; below 72, see pipe_min_blocks);
 //   Retrace bf16 10.26 / 9.30 / 10.30 / 11.15 / 11.40 / 9.21.
 // Prefetching whole rows before the wait floods L2 when the whole grid is resident at
 // once (one wave: every warp's row requested at the same moment). fp16 inputs move the
@@ -235,7 +236,10 @@ constexpr PipePrefetch pipe_prefetch()
                                                                     : PipePrefetch{256, 0};
     if (E == Est::kGae || E == Est::kTdLambda) return {256, 0};
     if (E == Est::kReturn) return {1024, 0};
-    return {512, 3};  // V-trace, Retrace
+    // V-trace and Retrace; with the 7-CTA cap bf16 V-trace prefers (256, 0): 11.90 vs
+    // 12.24 us, while fp16 V-trace (11.84 vs 12.19) and Retrace keep (512, 3).
+    if (E == Est::kVtrace && std::is_same<TIn, uint16_t>::value) return {256, 0};
+    return {512, 3};
 }
 
 template <Est E, typename TIn, bool MULTI = false>
@@ -250,12 +254,14 @@ void set_pipe_prefetch(Params &p)
 // scan (credit_warp_pipe_kernel). Rows longer than one warp chunk, 16-byte aligned.
 // CTAs per SM the register allocator must fit for the pipelined warp rows (0 = no
 // request). One warp per row must be resident at once: 4096 rows need 27 warps per SM on
-// GB300, 7 CTAs of 4 warps, at most 72 registers. fp16 widening costs registers that
-// bf16's shift does not (Retrace: 78-88 against 68-74), so fp16 asks for 7 CTAs per SM.
+// GB300, 7 CTAs of 4 warps, at most 72 registers. Uncapped, 16-bit V-trace needs 87-90
+// registers and fp16 Retrace 78-88 (5-6 CTAs per SM: two waves of warps), so the 16-bit
+// rows ask for 7 CTAs per SM (the others fit in 72 registers anyway). fp32 GAE and
+// TD(lambda) fit too; a cap was slower for the fused TD(lambda) (its own, in fused.cu).
 template <typename TIn>
 constexpr int pipe_min_blocks()
 {
-    return std::is_same<TIn, __half>::value ? 7 : 0;
+    return sizeof(TIn) == 2 ? 7 : 0;
 }
 
 template <Est E, int VEC, bool TRUNC, int DEPTH, typename TIn = float,
