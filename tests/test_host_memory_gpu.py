@@ -1,7 +1,7 @@
 """GPU parity with buffers in pinned host memory, which the kernels read and write in
 place over NVLink-C2C: every estimator with all buffers on the host, inputs only, or
-outputs only; the look-back path with host data and a device workspace; bf16 inputs;
-the fused TD(lambda) call and the forward scans. Buffers the device cannot reach
+outputs only; the look-back path with host data and a device workspace; bf16 and fp16
+inputs; the fused TD(lambda) call and the forward scans. Buffers the device cannot reach
 (pageable host memory, a host workspace) are refused before anything is launched."""
 import ctypes
 
@@ -12,7 +12,8 @@ import torch
 import oracle
 import segmented_associative_scan_gb300 as rlca
 import synthetic_rollouts as sr
-from parity_helpers import (ESTIMATORS, assert_parity, bf16_rounded, run_gpu, run_oracle)
+from parity_helpers import (ESTIMATORS, assert_parity, bf16_rounded, fp16_rounded, run_gpu,
+                            run_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +66,16 @@ def test_bf16_inputs_in_host_memory():
     for est in ESTIMATORS:
         assert_parity(run_gpu(est, ro, {}, in_dtype=torch.bfloat16, host="all"),
                       run_oracle(est, ro, {}), f"{est} bf16 host")
+
+
+@pytest.mark.parametrize("T", [200, 1024, 1500])
+def test_fp16_inputs_in_host_memory(T):
+    """fp16 inputs in pinned host memory: the CTA tiles (the pipelined rows are for
+    device memory) read them in place."""
+    ro = fp16_rounded(sr.generic(16, T, seed=10 + T))
+    for est in ESTIMATORS:
+        assert_parity(run_gpu(est, ro, {}, in_dtype=torch.float16, host="all"),
+                      run_oracle(est, ro, {}), f"{est} fp16 host T={T}")
 
 
 def _pinned(a):
