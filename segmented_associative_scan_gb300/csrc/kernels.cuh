@@ -645,6 +645,35 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(cons
     });
 }
 
+// Rows of exactly one warp chunk (T == 32 * ITEMS), more rows than warps one wave holds:
+// a grid of one wave in which each warp walks rows row0, row0 + stride, ... and asks for
+// the next row's raw words before it scans the current one, so its loads overlap its
+// own scans instead of waiting for a warp of a second wave to start. 16-byte aligned rows.
+template <Est E, int ITEMS, int VEC, bool TRUNC, int WARPS, typename TIn = float,
+          int MINB = 0>
+__global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_rows_pipe_kernel(const Params p)
+{
+    static_assert(VEC & kVec16, "raw chunks are read with vector loads");
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = (int64_t)gridDim.x * WARPS;
+    int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const int t0 = lane * ITEMS;
+    if (lane == 0) prefetch_row<E, TRUNC, TIn>(p, row, 0, p.T);
+    grid_dependency_sync();
+    if (row >= p.N) return;  // the whole warp leaves together
+    RawChunk<E, ITEMS, TIn> w;
+    load_raw<E, ITEMS, VEC, TRUNC>(p, row * p.ld, t0, lane, w);
+    while (true) {
+        Chunk<ITEMS> c;
+        unpack_raw<E, ITEMS, TRUNC>(w, p.T, t0, lane, c);
+        const int64_t next = row + stride;
+        if (next < p.N) load_raw<E, ITEMS, VEC, TRUNC>(p, next * p.ld, t0, lane, w);
+        warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, 0.f);
+        if (next >= p.N) break;
+        row = next;
+    }
+}
+
 // Fused TD(lambda) on pipelined warp-owned rows: each loaded chunk is scanned once per
 // lambda, each lambda with its own carry.
 template <int ITEMS, int VEC, bool TRUNC, int DEPTH, int WARPS = 4, int MINB = 0>

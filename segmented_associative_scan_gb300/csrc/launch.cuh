@@ -325,9 +325,58 @@ constexpr int warp_rows_items()
     return kItems;
 }
 
+// Rows of exactly one warp chunk with more rows than one wave of warps holds: one wave
+// of warps walking the rows with the next row's loads in flight
+// (credit_warp_rows_pipe_kernel), sized from the kernel's occupancy. Measured on GB300
+// at [8192, 256], us per launch, walked vs two waves of warp-owned rows: return 4.22 vs
+// 4.92, TD(lambda) 4.86 vs 5.75, GAE 7.10 vs 8.61; V-trace 11.84 vs 8.14 (its raw chunk
+// does not fit the 72 registers of its cap) and Retrace 7.92 vs 7.82 keep the waves.
+template <Est E>
+constexpr bool walk_rows_when_many()
+{
+    return E == Est::kReturn || E == Est::kTdLambda || E == Est::kGae;
+}
+
+template <Est E, int VEC, bool TRUNC, typename TIn = float>
+cudaError_t launch_warp_rows_pipe(Params p, cudaStream_t stream, bool *launched)
+{
+    constexpr int W = kWarpRowsPerCta;
+    constexpr int MINB = warp_min_blocks<E, TIn, kItems>();
+    auto kernel = credit_warp_rows_pipe_kernel<E, kItems, VEC, TRUNC, W, TIn, MINB>;
+    static std::atomic<int> per_sm_cache{0};
+    int per_sm = per_sm_cache.load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * W, 0) !=
+                cudaSuccess || per_sm <= 0) {
+            (void)cudaGetLastError();
+            *launched = false;
+            return cudaSuccess;
+        }
+        per_sm_cache.store(per_sm, std::memory_order_relaxed);
+    }
+    const int64_t wave = (int64_t)per_sm * sm_count();  // CTAs resident at once
+    const int64_t ctas = (p.N + W - 1) / W;
+    if (ctas <= wave) {  // one wave already: nothing to walk
+        *launched = false;
+        return cudaSuccess;
+    }
+    p.segs = 1;
+    p.chunks_per_row = 32;
+    p.rows_per_tile = 1;
+    *launched = true;
+    return launch_pdl(kernel, (unsigned)wave, 32 * W, 0, stream, p);
+}
+
 template <Est E, int VEC, bool TRUNC>
 cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
 {
+    if constexpr (walk_rows_when_many<E>() && (VEC & kVec16) != 0) {
+        if (path == Path::kWarpRows && p.T == 32 * kItems && !p.host) {
+            bool launched = false;
+            const cudaError_t err = launch_warp_rows_pipe<E, VEC, TRUNC>(p, stream, &launched);
+            if (launched || err != cudaSuccess) return err;
+        }
+    }
     if (path == Path::kWarpRows) {
         constexpr int I = warp_rows_items<E>();
         if (I != kItems && p.T <= 32 * I)

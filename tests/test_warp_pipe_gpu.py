@@ -79,3 +79,15 @@ def test_parameters(params):
         q = {k: v for k, v in params.items() if est != "return" or k == "gamma"}
         assert_parity(run_gpu(est, rb, q, in_dtype=BF), run_oracle(est, rb, q),
                       f"{est} bf16 {q}")
+
+
+@pytest.mark.parametrize("ld_extra,offset", [(0, 0), (8, 0), (4, 0), (0, 4)])
+@pytest.mark.parametrize("N", [9001, 12288])
+def test_rows_walked_by_one_wave(N, ld_extra, offset):
+    """Rows of exactly 256 steps, more of them than one wave of warps holds: one wave of
+    warps walks the rows, each loading its next row while it scans the current one. Row
+    counts that do not divide the grid, and padded or offset layouts."""
+    ro = sr.generic(N, 256, seed=6000 + N + ld_extra, p_term=0.01, p_trunc=0.01)
+    for est in ESTIMATORS:
+        assert_parity(run_gpu(est, ro, {}, ld=256 + ld_extra, offset=offset),
+                      run_oracle(est, ro, {}), f"{est} N={N} ld+{ld_extra} off={offset}")
