@@ -119,9 +119,11 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
         if workspace and N < 2 * sms:
             return f"credit_scan_kernel<{name}, look-back across CTA tiles>"
         return f"credit_scan_kernel<{name}, CTA row loop>"
-    if T == 256 and be in ("return", "td_lambda", "gae") and N * T > 4096 * 256:
-        return (f"credit_warp_rows_pipe_kernel<{name}> (one wave of warps walking the rows, "
-                "the next row's loads in flight)")
+    if (T in (64, 128, 256) and N % (256 // T) == 0 and be in ("return", "td_lambda", "gae")
+            and N * T > 4096 * 256):
+        rows = "the rows" if T == 256 else f"blocks of {256 // T} rows"
+        return (f"credit_warp_rows_pipe_kernel<{name}> (one wave of warps walking {rows}, "
+                "the next block's loads in flight)")
     if T <= 256:
         return f"credit_warp_kernel<{name}> (warp-owned rows)"
     if be == "gae" or (be == "td_lambda" and T > 512):

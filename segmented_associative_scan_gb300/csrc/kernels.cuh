@@ -645,10 +645,12 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(cons
     });
 }
 
-// Rows of exactly one warp chunk (T == 32 * ITEMS), more rows than warps one wave holds:
-// a grid of one wave in which each warp walks rows row0, row0 + stride, ... and asks for
-// the next row's raw words before it scans the current one, so its loads overlap its
-// own scans instead of waiting for a warp of a second wave to start. 16-byte aligned rows.
+// Rows that tile one warp chunk exactly (rows_per_tile rows of T steps, T * rows_per_tile
+// == 32 * ITEMS, contiguous when there are several), more of these jobs than one wave of
+// warps holds: a grid of one wave in which each warp walks jobs j, j + stride, ... and
+// asks for the next job's raw words before it scans the current one, so its loads
+// overlap its own scans instead of waiting for a warp of a second wave to start.
+// 16-byte aligned rows; N a multiple of rows_per_tile.
 template <Est E, int ITEMS, int VEC, bool TRUNC, int WARPS, typename TIn = float,
           int MINB = 0>
 __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_rows_pipe_kernel(const Params p)
@@ -656,21 +658,27 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_rows_pipe_kernel
     static_assert(VEC & kVec16, "raw chunks are read with vector loads");
     const int lane = threadIdx.x & 31;
     const int64_t stride = (int64_t)gridDim.x * WARPS;
-    int64_t row = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
-    const int t0 = lane * ITEMS;
-    if (lane == 0) prefetch_row<E, TRUNC, TIn>(p, row, 0, p.T);
+    const int64_t jobs = p.N / p.rows_per_tile;
+    int64_t job = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const LaneSlot ls = lane_slot(p, lane);
+    const int t0 = ls.chunk * ITEMS;  // within the lane's row
+    const int tb = lane * ITEMS;      // within the job's block of rows
+    if (lane < p.rows_per_tile)
+        prefetch_row<E, TRUNC, TIn>(p, job * p.rows_per_tile + lane, 0, p.T);
     grid_dependency_sync();
-    if (row >= p.N) return;  // the whole warp leaves together
+    if (job >= jobs) return;  // the whole warp leaves together
     RawChunk<E, ITEMS, TIn> w;
-    load_raw<E, ITEMS, VEC, TRUNC>(p, row * p.ld, t0, lane, w);
+    load_raw<E, ITEMS, VEC, TRUNC>(p, job * p.rows_per_tile * p.ld, tb, lane, w);
     while (true) {
         Chunk<ITEMS> c;
         unpack_raw<E, ITEMS, TRUNC>(w, p.T, t0, lane, c);
-        const int64_t next = row + stride;
-        if (next < p.N) load_raw<E, ITEMS, VEC, TRUNC>(p, next * p.ld, t0, lane, w);
-        warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, 0.f);
-        if (next >= p.N) break;
-        row = next;
+        const int64_t next = job + stride;
+        if (next < jobs)
+            load_raw<E, ITEMS, VEC, TRUNC>(p, next * p.rows_per_tile * p.ld, tb, lane, w);
+        warp_chunk_scan<E, ITEMS, VEC, TIn>(p, job * p.rows_per_tile + ls.local_row, t0, c,
+                                            0.f);
+        if (next >= jobs) break;
+        job = next;
     }
 }
 

@@ -325,12 +325,16 @@ constexpr int warp_rows_items()
     return kItems;
 }
 
-// Rows of exactly one warp chunk with more rows than one wave of warps holds: one wave
-// of warps walking the rows with the next row's loads in flight
-// (credit_warp_rows_pipe_kernel), sized from the kernel's occupancy. Measured on GB300
-// at [8192, 256], us per launch, walked vs two waves of warp-owned rows: return 4.22 vs
-// 4.92, TD(lambda) 4.86 vs 5.75, GAE 7.10 vs 8.61; V-trace 11.84 vs 8.14 (its raw chunk
-// does not fit the 72 registers of its cap) and Retrace 7.92 vs 7.82 keep the waves.
+// Rows that tile one warp chunk (256 steps: one row, or 2 or 4 contiguous rows of 128 or
+// 64 steps), more such jobs than one wave of warps holds: one wave of warps walking the
+// jobs with the next job's loads in flight (credit_warp_rows_pipe_kernel), sized from the
+// kernel's occupancy. Measured on GB300, us per launch, walked vs warp-owned rows in
+// waves: [8192, 256] return 4.22 vs 4.92, TD(lambda) 4.86 vs 5.75, GAE 7.10 vs 8.61;
+// [16384, 128] return 4.33 vs 4.99, TD(lambda) 4.86 vs 5.76, GAE 7.02 vs 8.40; [32768, 64]
+// return 4.48 vs 5.06. V-trace 11.84 vs 8.14 (its raw chunk does not fit
+// the 72 registers of its cap) and Retrace 7.92 vs 7.82 keep the waves. Jobs that fit
+// one wave gain nothing: half the warps walking two jobs each took return [4096, 128]
+// from 2.19 to 2.91 us.
 template <Est E>
 constexpr bool walk_rows_when_many()
 {
@@ -355,14 +359,16 @@ cudaError_t launch_warp_rows_pipe(Params p, cudaStream_t stream, bool *launched)
         per_sm_cache.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t wave = (int64_t)per_sm * sm_count();  // CTAs resident at once
-    const int64_t ctas = (p.N + W - 1) / W;
+    const int rpt = 32 * kItems / p.T;                  // rows per job
+    const int64_t ctas = (p.N / rpt + W - 1) / W;
     if (ctas <= wave) {  // one wave already: nothing to walk
         *launched = false;
         return cudaSuccess;
     }
     p.segs = 1;
-    p.chunks_per_row = 32;
-    p.rows_per_tile = 1;
+    p.chunks_per_row = p.T / kItems;
+    p.rows_per_tile = rpt;
+    set_lane_split(p);
     *launched = true;
     return launch_pdl(kernel, (unsigned)wave, 32 * W, 0, stream, p);
 }
@@ -371,7 +377,12 @@ template <Est E, int VEC, bool TRUNC>
 cudaError_t launch_path(const Params &p, Path path, cudaStream_t stream)
 {
     if constexpr (walk_rows_when_many<E>() && (VEC & kVec16) != 0) {
-        if (path == Path::kWarpRows && p.T == 32 * kItems && !p.host) {
+        // Jobs of whole contiguous rows: T divides the warp chunk, rows packed when
+        // several share a job (ld == T), N a multiple of the rows per job.
+        const bool tiles = p.T == 32 * kItems ||
+                           ((p.T == 16 * kItems || p.T == 8 * kItems) && p.ld == p.T &&
+                            p.N % (32 * kItems / p.T) == 0);
+        if (path == Path::kWarpRows && tiles && !p.host) {
             bool launched = false;
             const cudaError_t err = launch_warp_rows_pipe<E, VEC, TRUNC>(p, stream, &launched);
             if (launched || err != cudaSuccess) return err;

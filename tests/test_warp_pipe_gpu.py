@@ -91,3 +91,13 @@ def test_rows_walked_by_one_wave(N, ld_extra, offset):
     for est in ESTIMATORS:
         assert_parity(run_gpu(est, ro, {}, ld=256 + ld_extra, offset=offset),
                       run_oracle(est, ro, {}), f"{est} N={N} ld+{ld_extra} off={offset}")
+
+
+@pytest.mark.parametrize("N,T", [(20000, 128), (40000, 64), (20002, 128)])
+def test_packed_rows_walked_by_one_wave(N, T):
+    """Rows of 128 or 64 steps packed two or four to a warp chunk (contiguous, ld == T),
+    more such jobs than one wave holds: the walked rows. An odd number of jobs per warp
+    and, for [20002, 128], jobs that do not divide the grid."""
+    ro = sr.generic(N, T, seed=7000 + N + T, p_term=0.02, p_trunc=0.01)
+    for est in ("return", "td_lambda", "gae"):
+        assert_parity(run_gpu(est, ro, {}), run_oracle(est, ro, {}), f"{est} N={N} T={T}")
