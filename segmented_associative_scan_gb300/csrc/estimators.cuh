@@ -103,6 +103,8 @@ struct Chunk {
     float y[ITEMS];
     float sv[ITEMS];  // successor value where the episode stops (V-trace keeps it)
     float v_next, x_next, y_next;
+    float boot_v;    // the per-env bootstrap if the thread holds the row's last step, else 0
+    bool boot_late;  // boot_v unset: build() reads the bootstrap once the flags are in
     unsigned stop;   // bit j: the recursion stops at step j (boundary or padding)
     unsigned term;   // bit j: step j terminated
     unsigned trunc;  // bit j: step j truncated
@@ -148,7 +150,21 @@ __device__ __forceinline__ float next_item(float first_item, const TIn *__restri
     return need ? s : 0.f;
 }
 
-template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float>
+// The per-env bootstrap (successor value at the window end, Method section 3) for a
+// thread whose items t0 .. t0+ITEMS-1 hold the row's last step, else 0. Its address needs
+// no loaded data, so it is read together with the chunk's data instead of after the
+// chunk's flags arrive (that would put a second memory latency on the thread's path).
+template <int ITEMS>
+__device__ __forceinline__ float load_boot(const Params &p, int64_t row, int t0, bool active)
+{
+    const int last = p.T - 1 - t0;
+    return (active && p.boot && last >= 0 && last < ITEMS) ? __ldg(p.boot + row) : 0.f;
+}
+
+// EARLY_BOOT: the bootstrap is read with the data (load_boot); else build() reads it
+// where it is used, once the chunk's flags are in (a second memory latency on the
+// thread's path, but no register held from the load to the use).
+template <Est E, int ITEMS, int VEC, bool TRUNC, typename TIn = float, bool EARLY_BOOT = true>
 __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0, bool active,
                                            int lane, Chunk<ITEMS> &c)
 {
@@ -157,6 +173,8 @@ __device__ __forceinline__ void load_chunk(const Params &p, int64_t row, int t0,
     const int Te = active ? T : 0;  // an inactive thread sees an empty row
     const int64_t off = active ? row * p.ld : 0;
 
+    c.boot_v = EARLY_BOOT ? load_boot<ITEMS>(p, row, t0, active) : 0.f;
+    c.boot_late = !EARLY_BOOT;
     load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.reward, off), t0, Te, c.r);
     if (Tr::kValue) load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.value, off), t0, Te, c.v);
     if (Tr::kAux) load_items<ITEMS, VEC, TIn>(in_row<TIn>(p.aux, off), t0, Te, c.x);
@@ -272,13 +290,16 @@ __device__ __forceinline__ void widen_words(const uint32_t (&w)[kWords], float (
                             x + PV * k);
 }
 
-// A full chunk's Chunk from its raw words (what load_chunk forms from its loads).
+// A full chunk's Chunk from its raw words (what load_chunk forms from its loads);
+// boot_v: load_boot of the thread's items, read when the raw words were requested.
 // Every thread of the warp must call this (it shuffles).
 template <Est E, int ITEMS, bool TRUNC, typename TIn>
 __device__ __forceinline__ void unpack_raw(const RawChunk<E, ITEMS, TIn> &w, int T, int t0,
-                                           int lane, Chunk<ITEMS> &c)
+                                           int lane, float boot_v, Chunk<ITEMS> &c)
 {
     using Tr = EstTraits<E>;
+    c.boot_v = boot_v;
+    c.boot_late = false;
     widen_words<TIn>(w.r, c.r);
     if constexpr (Tr::kValue) widen_words<TIn>(w.v, c.v);
     if constexpr (Tr::kAux) widen_words<TIn>(w.x, c.x);
@@ -337,7 +358,8 @@ __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chun
             if (load_sv & (1u << j))
                 c.sv[j] = (c.trunc & (1u << j))
                               ? InType<TIn>::cached(in_row<TIn>(p.trunc_value, off) + t0 + j)
-                              : (p.boot ? __ldg(p.boot + row) : 0.f);
+                              : c.boot_late ? (p.boot ? __ldg(p.boot + row) : 0.f)
+                                            : c.boot_v;
     }
 #pragma unroll
     for (int j = 0; j < ITEMS; ++j) {

@@ -34,6 +34,8 @@
 // pipelined form (a warp per row that keeps the next chunks' loads in flight).
 #pragma once
 
+#include <type_traits>
+
 #include "estimators.cuh"
 
 namespace rlca {
@@ -213,14 +215,16 @@ __device__ __forceinline__ float scan_chunk(const Params &p, Chunk<ITEMS> &c, in
     return tile_first;
 }
 
-// Load this thread's steps from global memory, then scan_chunk.
-template <Est E, int NT, int ITEMS, int VEC, bool TRUNC, bool LB, typename TIn = float>
+// Load this thread's steps from global memory, then scan_chunk. EARLY_BOOT: as in
+// load_chunk.
+template <Est E, int NT, int ITEMS, int VEC, bool TRUNC, bool LB, typename TIn = float,
+          bool EARLY_BOOT = true>
 __device__ __forceinline__ float scan_tile(const Params &p, int64_t row, int t0, bool active,
                                            float carry_in, ScanSmem<NT> &sm, int buf,
                                            int seg = 0, unsigned epoch = 0)
 {
     Chunk<ITEMS> c;
-    load_chunk<E, ITEMS, VEC, TRUNC, TIn>(p, row, t0, active, threadIdx.x & 31, c);
+    load_chunk<E, ITEMS, VEC, TRUNC, TIn, EARLY_BOOT>(p, row, t0, active, threadIdx.x & 31, c);
     return scan_chunk<E, NT, ITEMS, VEC, LB, TIn>(p, c, row, t0, carry_in, sm, buf, seg, epoch);
 }
 
@@ -299,12 +303,14 @@ __global__ void __launch_bounds__(NT, MINB) credit_scan_kernel(const Params p)
         scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn>(p, blockIdx.x, threadIdx.x * ITEMS, true,
                                                         0.f, sm, 0);
     } else if (TL == Tiling::kRowLoop) {
+        // The bootstrap is read late here: reading it with the last tile's data was
+        // measured slower (Retrace [2048, 4096] 26.8 vs 25.8 us).
         const int64_t row = blockIdx.x;
         float carry = 0.f;
         for (int s = p.segs - 1; s >= 0; --s) {
             if (threadIdx.x == 0 && s > 0)  // the next tile's reads overlap this tile
                 prefetch_row<E, TRUNC, TIn>(p, row, (s - 1) * TILE, s * TILE);
-            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn>(
+            carry = scan_tile<E, NT, ITEMS, VEC, TRUNC, false, TIn, false>(
                 p, row, s * TILE + threadIdx.x * ITEMS, true, carry, sm, s & 1);
         }
     } else {
@@ -589,8 +595,10 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_kernel(const Par
 // pipeline), so its HBM reads overlap its own scans and stores instead of alternating
 // with them. A ragged last chunk goes first through the plain load, before the
 // pipeline starts; every chunk after that is full. scan(t0, c) scans one loaded chunk
-// (thread's first step t0). Needs 16-byte aligned rows (VEC >= 1).
-template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, typename TIn, typename Scan>
+// (thread's first step t0). Needs 16-byte aligned rows (VEC >= 1). BOOT: how the
+// bootstrap of the row's end is read (pipe_boot_mode).
+template <Est E, int ITEMS, int VEC, bool TRUNC, int DEPTH, typename TIn, int BOOT,
+          typename Scan>
 __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan &&scan)
 {
     static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three chunks in flight");
@@ -606,26 +614,56 @@ __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan
         --s;
     }
     if (s < 0) return;
+    // The row's last step is in chunk s unless a ragged chunk took it above.
+    const float boot = BOOT > 0 ? load_boot<ITEMS>(p, row, s * CH + lane * ITEMS, true) : 0.f;
     // w[d] holds chunk s - d (registers: every index below is a compile-time constant).
     RawChunk<E, ITEMS, TIn> w[DEPTH];
 #pragma unroll
     for (int d = 0; d < DEPTH; ++d)
         if (s - d >= 0)
             load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - d) * CH + lane * ITEMS, lane, w[d]);
-    for (; s >= 0; --s) {
-        const int t0 = s * CH + lane * ITEMS;
-        if (lane == 0 && p.pf_ahead > 0 && s >= p.pf_ahead)  // beyond the registers' reach
-            prefetch_row<E, TRUNC, TIn>(p, row, (s - p.pf_ahead) * CH,
-                                        (s - p.pf_ahead + 1) * CH);
+    auto step = [&](int k, float boot_v) {
+        const int t0 = k * CH + lane * ITEMS;
+        if (lane == 0 && p.pf_ahead > 0 && k >= p.pf_ahead)  // beyond the registers' reach
+            prefetch_row<E, TRUNC, TIn>(p, row, (k - p.pf_ahead) * CH,
+                                        (k - p.pf_ahead + 1) * CH);
         Chunk<ITEMS> c;
-        unpack_raw<E, ITEMS, TRUNC>(w[0], p.T, t0, lane, c);
+        unpack_raw<E, ITEMS, TRUNC>(w[0], p.T, t0, lane, boot_v, c);
+        c.boot_late = BOOT == 0;
 #pragma unroll
         for (int d = 0; d + 1 < DEPTH; ++d) w[d] = w[d + 1];
-        if (s - DEPTH >= 0)
-            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (s - DEPTH) * CH + lane * ITEMS, lane,
+        if (k - DEPTH >= 0)
+            load_raw<E, ITEMS, VEC, TRUNC>(p, off, (k - DEPTH) * CH + lane * ITEMS, lane,
                                            w[DEPTH - 1]);
         scan(t0, c);
+    };
+    if (BOOT == 2) {  // the first chunk scanned holds the row's end; the rest need no value
+        step(s, boot);
+        --s;
     }
+    for (; s >= 0; --s) step(s, BOOT == 1 ? boot : 0.f);
+}
+
+// How the pipelined rows read the per-env bootstrap (the successor value of the row's
+// last step, in the first chunk they scan): 0, once that chunk's flags are in (a second
+// memory latency on the warp's path, no register held); 1, together with the chunk's
+// raw words (load_boot; the value is held through the walk); 2, the same with the first
+// chunk's step peeled off the loop, so the value is dead after it (a second copy of the
+// scan code). Measured on GB300 at [4096, 1024], us per launch for modes 0 / 1 / 2:
+// fp32 TD(lambda) 9.33 / 9.05 / 9.02, GAE 12.29 / 12.31 / 12.31; bf16 TD(lambda)
+// 7.99 / 7.79 / 7.01, GAE 11.00 / 10.90 / 10.45, V-trace 11.89 / 11.54 / 11.70, Retrace
+// 9.17 / 8.96 / 9.43; fp16 TD(lambda) 7.40 / 7.60 / 7.50, GAE 10.89 / 10.74 / 10.43,
+// V-trace 11.89 / 12.36 / 12.27, Retrace 9.91 / 9.02 / 9.20; fused TD(lambda) 14.40 /
+// 14.53 / 14.55. The differences follow the register allocation of each kernel more
+// than the latency itself.
+template <Est E, typename TIn>
+__host__ __device__ constexpr int pipe_boot_mode()
+{
+    if (sizeof(TIn) == 4) return E == Est::kTdLambda ? 2 : 0;
+    if (E == Est::kVtrace || E == Est::kRetrace)
+        return (E == Est::kVtrace && !std::is_same<TIn, uint16_t>::value) ? 0 : 1;
+    if (E == Est::kTdLambda && !std::is_same<TIn, uint16_t>::value) return 0;
+    return 2;
 }
 
 // Pipelined warp-owned rows (warp_pipe_row): one row per warp, T > 32 * ITEMS. MINB:
@@ -640,7 +678,8 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_pipe_kernel(cons
     grid_dependency_sync();
     if (row >= p.N) return;  // the whole warp leaves together
     float carry = 0.f;
-    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, TIn>(p, row, [&](int t0, Chunk<ITEMS> &c) {
+    constexpr int BOOT = pipe_boot_mode<E, TIn>();
+    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, TIn, BOOT>(p, row, [&](int t0, Chunk<ITEMS> &c) {
         carry = warp_chunk_scan<E, ITEMS, VEC, TIn>(p, row, t0, c, carry);
     });
 }
@@ -667,14 +706,24 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_warp_rows_pipe_kernel
         prefetch_row<E, TRUNC, TIn>(p, job * p.rows_per_tile + lane, 0, p.T);
     grid_dependency_sync();
     if (job >= jobs) return;  // the whole warp leaves together
+    // The bootstrap of each job's rows is read with its raw words, except for GAE, which
+    // reads it once the flags are in (walked rows at [8192, 256], us per launch, late vs
+    // early: return 4.22 vs 3.86, TD(lambda) 4.82 vs 4.56, GAE 7.06 vs 7.18).
+    constexpr bool EARLY = E != Est::kGae;
     RawChunk<E, ITEMS, TIn> w;
     load_raw<E, ITEMS, VEC, TRUNC>(p, job * p.rows_per_tile * p.ld, tb, lane, w);
+    float boot = EARLY ? load_boot<ITEMS>(p, job * p.rows_per_tile + ls.local_row, t0, true)
+                       : 0.f;
     while (true) {
         Chunk<ITEMS> c;
-        unpack_raw<E, ITEMS, TRUNC>(w, p.T, t0, lane, c);
+        unpack_raw<E, ITEMS, TRUNC>(w, p.T, t0, lane, boot, c);
+        c.boot_late = !EARLY;
         const int64_t next = job + stride;
-        if (next < jobs)
+        if (next < jobs) {
             load_raw<E, ITEMS, VEC, TRUNC>(p, next * p.rows_per_tile * p.ld, tb, lane, w);
+            if (EARLY)
+                boot = load_boot<ITEMS>(p, next * p.rows_per_tile + ls.local_row, t0, true);
+        }
         warp_chunk_scan<E, ITEMS, VEC, TIn>(p, job * p.rows_per_tile + ls.local_row, t0, c,
                                             0.f);
         if (next >= jobs) break;
@@ -694,7 +743,7 @@ __global__ void __launch_bounds__(32 * WARPS, MINB) credit_td_multi_pipe_kernel(
     grid_dependency_sync();
     if (row >= p.N) return;
     float carry[kMaxLambdas] = {0.f, 0.f, 0.f, 0.f};
-    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, float>(p, row, [&](int t0, Chunk<ITEMS> &c) {
+    warp_pipe_row<E, ITEMS, VEC, TRUNC, DEPTH, float, 0>(p, row, [&](int t0, Chunk<ITEMS> &c) {
 #pragma unroll
         for (int k = 0; k < kMaxLambdas; ++k) {
             if (k < p.multi.count) {
