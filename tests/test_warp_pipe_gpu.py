@@ -101,3 +101,27 @@ def test_packed_rows_walked_by_one_wave(N, T):
     ro = sr.generic(N, T, seed=7000 + N + T, p_term=0.02, p_trunc=0.01)
     for est in ("return", "td_lambda", "gae"):
         assert_parity(run_gpu(est, ro, {}), run_oracle(est, ro, {}), f"{est} N={N} T={T}")
+
+
+@pytest.mark.parametrize("fmt", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("N,T", [(40, 128), (9001, 256), (37, 1024), (9, 2100)])
+def test_bootstrap_read_early_or_late(N, T, fmt):
+    """The per-env bootstrap is read beside a chunk's data on some paths and only once the
+    flags are in on others (the row loops, some pipelined rows). Every layout (warp-owned
+    rows, walked rows, pipelined or CTA rows, the row loop) in every input format: without
+    a bootstrap, and with one while the last step is truncated (its truncation value wins)
+    or terminated (no successor value)."""
+    from parity_helpers import fp16_rounded
+    dtype = {"fp32": torch.float32, "bf16": BF, "fp16": torch.float16}[fmt]
+    rnd = {"fp32": lambda r: r, "bf16": bf16_rounded, "fp16": fp16_rounded}[fmt]
+    for case in ("no bootstrap", "truncated last step", "terminated last step"):
+        ro = rnd(sr.generic(N, T, seed=8000 + N + T, p_term=0.01, p_trunc=0.01))
+        if case == "no bootstrap":
+            ro.bootstrap = None
+        elif case == "truncated last step":
+            ro.truncated[::2, -1] = 1
+        else:
+            ro.terminated[1::2, -1] = 1
+        for est in ESTIMATORS:
+            assert_parity(run_gpu(est, ro, {}, in_dtype=dtype), run_oracle(est, ro, {}),
+                          f"{est} {fmt} N={N} T={T} {case}")
