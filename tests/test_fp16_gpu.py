@@ -118,3 +118,19 @@ def test_fp16_rejects_mixed_dtypes_and_workspace():
         rlca.rlca_gae(r, torch.zeros((4, 2048), device=dev, dtype=torch.float32), d)
     with pytest.raises(ValueError):
         rlca.rlca_gae(r, r, d, workspace=torch.zeros(4096, dtype=torch.uint8, device=dev))
+
+
+def test_every_half_pattern_widens_exactly():
+    """Every binary16 bit pattern the fp16 entry points read is widened to the exact
+    binary32 value (compared with torch's CPU conversion, NaNs as NaNs): an eligibility
+    trace whose every step terminates returns its inputs unchanged."""
+    x = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(HF).reshape(256, 256)
+    want = x.float()
+    dev = torch.device("cuda")
+    term = torch.ones((256, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((256, 256), dtype=torch.float32, device=dev)
+    rlca.rlca_eligibility_trace(x.to(dev), term, None, None, decay=0.9, traces=out)
+    got = out.cpu()
+    nan = torch.isnan(want)
+    assert torch.equal(torch.isnan(got), nan)
+    assert torch.equal(got[~nan].view(torch.int32), want[~nan].view(torch.int32))
