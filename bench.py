@@ -160,6 +160,13 @@ NCU_TRAFFIC = {
     (_H, "gae", 8192, 256, False): 38_319_872,
     (_H, "return", 16384, 128, False): 18_952_960,
     (_H, "return", 16, 524288, True): 76_033_568,
+    (_H, "td_multi", 4096, 128, False): 11_046_400,
+    (_H, "td_lambda", 4096, 128, False): 6_850_560,
+    (_H, "gae", 16, 128, False): 61_952,
+    (_H, "trace", 4096, 128, False): 5_275_648,
+    (_H, "td_lambda_bf16", 4096, 1024, False): 38_135_680,
+    (_H, "retrace_bf16", 4096, 1024, False): 56_088_960,
+    (_H, "trace_bf16", 4096, 1024, False): 35_104_512,
 }
 
 
