@@ -340,7 +340,8 @@ __device__ __forceinline__ float at_or_next(const float (&a)[ITEMS], float next,
 // Forms (alpha, beta) of every item: one select picks the value of the state after the
 // step (the next step's value inside an episode, the successor value where it stops),
 // one picks beta or the reset marker. Successor values that need a load (truncated
-// steps and the window end) are fetched in a branch that few threads take.
+// steps, and the window end where its bootstrap was not read with the data, boot_late)
+// are fetched in a branch that few threads take.
 // V-trace keeps rho_t in c.x for the epilogue.
 template <Est E, int ITEMS, typename TIn = float>
 __device__ __forceinline__ void build(const Params &p, int64_t row, int t0, Chunk<ITEMS> &c,
