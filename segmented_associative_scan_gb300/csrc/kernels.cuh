@@ -30,8 +30,12 @@
 //
 // Also here: the fused kernels (TD(lambda) for several lambdas, GAE with V-trace: one
 // load of a tile, one scan per estimator), the warp-owned-rows kernel (a warp scans
-// whole short rows, or walks a row in warp-sized chunks, with no CTA barrier) and its
-// pipelined form (a warp per row that keeps the next chunks' loads in flight).
+// whole short rows, or walks a row in warp-sized chunks, with no CTA barrier), its
+// pipelined form (a warp per row that keeps the next chunks' loads in flight) and the
+// walked rows (a grid of one wave whose warps walk blocks of short rows, the next
+// block's loads in flight). Where a thread holds a row's last step, the per-env
+// bootstrap is read beside its data on most paths (load_boot), late where that measured
+// faster (pipe_boot_mode, the row loops).
 #pragma once
 
 #include <type_traits>
