@@ -104,7 +104,7 @@ def test_packed_rows_walked_by_one_wave(N, T):
 
 
 @pytest.mark.parametrize("fmt", ["fp32", "bf16", "fp16"])
-@pytest.mark.parametrize("N,T", [(40, 128), (9001, 256), (37, 1024), (9, 2100)])
+@pytest.mark.parametrize("N,T", [(40, 128), (9001, 256), (20000, 128), (37, 1024), (9, 2100)])
 def test_bootstrap_read_early_or_late(N, T, fmt):
     """The per-env bootstrap is read beside a chunk's data on some paths and only once the
     flags are in on others (the row loops, some pipelined rows). Every layout (warp-owned
