@@ -497,6 +497,9 @@ def time_workload(torch, rlca, device, peak, est, ro, ceiling=True):
            "frac_of_8tbs": round(gbs / 8000.0, 4),
            "timesteps_per_s": round(ro.N * ro.T / (us * 1e-6), 1),
            "inputs_exceed_l2": n_sets * nbytes > L2_BYTES}
+    traffic = NCU_TRAFFIC.get((kernel_source_hash(), est, ro.N, ro.T, False))
+    if traffic is not None:  # bytes one captured launch moved, against the algorithmic
+        out["ncu_traffic_ratio"] = round(traffic / nbytes, 3)
     if ceiling:
         # The best plain copy of the same bytes: in the kernel's launch shape, and for a
         # kernel that walks rows per warp also in the flat shape (one chunk per warp).
@@ -889,8 +892,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         if args.detail:
             with open(args.detail, "w") as f:
                 json.dump({"configs": configs, "estimators": estimators}, f, indent=1)
-        keep = ("us_per_launch", "frac", "ceiling_us", "frac_of_ceiling", "inputs_exceed_l2",
-                "oracle_timesteps_per_s")
+        keep = ("us_per_launch", "frac", "ceiling_us", "frac_of_ceiling", "ncu_traffic_ratio",
+                "inputs_exceed_l2", "oracle_timesteps_per_s")
         result["configs"] = {k: {f: v[f] for f in keep if f in v} for k, v in configs.items()}
         # Last key: each estimator alone at [4096, 1024], us per launch, fraction of the
         # measured peak and of its plain-copy ceiling.
