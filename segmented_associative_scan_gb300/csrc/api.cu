@@ -135,7 +135,7 @@ int validate_and_launch(Params &p, const float *const *f32_in, int n_in, float *
         if (p.spin_limit <= 0) p.spin_limit = rlca::kDefaultSpinLimit;
     }
 
-    // Checked last, as it asks the driver: every buffer must be reachable from the
+    // Checked last, as it asks the CUDA runtime: every buffer must be reachable from the
     // current device. Pinned host memory is read and written in place (no bulk copies
     // from it: the kernels then use plain loads and stores).
     int device = 0;
