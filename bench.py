@@ -88,8 +88,10 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
     if be in ("trace", "prefix_sum"):
         if T <= 256:
             return "credit_forward_kernel (warp-owned rows, forward)"
-        return ("credit_forward_pipe_kernel (a warp per row walking forward, 2 chunks of "
-                "loads in flight)" if T <= 1024
+        ctas = (N + 3) // 4
+        depth = 3 if narrow or 9 * sms <= 2 * ctas <= 14 * sms else 2
+        return (f"credit_forward_pipe_kernel (a warp per row walking forward, {depth} chunks "
+                "of loads in flight)" if T <= 1024
                 else "credit_forward_tile_kernel (CTA row loop, forward)")
     if be == "td_multi":
         if T <= 256:
@@ -126,6 +128,9 @@ def kernel_desc(est: str, N: int, T: int, workspace: bool, sms: int) -> str:
                 "the next block's loads in flight)")
     if T <= 256:
         return f"credit_warp_kernel<{name}> (warp-owned rows)"
+    if be == "return" and 512 < T <= 960 and (N + 3) // 4 <= 7 * sms:
+        return (f"credit_warp_pipe_kernel<{name}> (a warp per row, 2 chunks of loads in "
+                "flight, 7 CTAs per SM)")
     if be == "gae" or (be == "td_lambda" and T > 512):
         return f"credit_warp_pipe_kernel<{name}> (a warp per row, next chunk's loads in flight)"
     return f"credit_scan_kernel<{name}, whole-row CTA tiles>"

@@ -19,6 +19,14 @@ namespace rlca {
 // 1024 steps 7.66 / 7.55 (bf16 7.47 / 7.57, fp16 7.87 / 7.89); three chunks (fp32 1024
 // steps, bf16 1024, fp16 256): fp32 8.08 / 8.07, bf16 7.06 / 7.07 against 7.29 / 7.29
 // with two, fp16 7.36 / 7.36 against 7.61 / 7.62 (fp32 58-64 registers, one wave still).
+// fp32 rows take three chunks too, under a 7-CTA cap (68 registers), where the grid
+// fills most of one wave of warps at that cap (4.5 to 7 CTAs per SM). Eligibility
+// trace, us per launch, two chunks uncapped -> three capped: [N, 1024] for N = 2200
+// 5.54 -> 5.54, 2432 5.80 -> 5.80, 2440 5.81 -> 6.57, 2600 5.96 -> 6.71, 2800 7.09 ->
+// 6.79, 3000 7.19 -> 6.85, 3200 7.24 -> 6.94, 3600 7.28 -> 7.16, 4000 7.47 -> 7.28,
+// 4096 7.57 -> 7.32, 4256 7.66 -> 7.46, 8192 13.62 -> 14.34 (two waves); [4096, 600]
+// 7.07 -> 6.30. Each form steps up where its CTAs per SM pass 4 (three chunks) or about
+// 4.4 (two).
 struct ForwardPipe {
     int depth, first, ahead, pipe_from;
 };
@@ -48,6 +56,14 @@ cudaError_t launch_forward_variant(Params p, cudaStream_t stream)
             p.pf_first = fp.first;
             p.pf_ahead = fp.ahead;
             const unsigned grid = (unsigned)((p.N + kWarpsPerCta - 1) / kWarpsPerCta);
+            if constexpr (sizeof(TIn) == 4) {
+                constexpr int kCap = 7;  // CTAs of 4 warps per SM: 72 registers
+                const int64_t sms = sm_count();
+                if (2 * (int64_t)grid >= 9 * sms && (int64_t)grid <= kCap * sms)
+                    return launch_pdl(credit_forward_pipe_kernel<kItems, kVec16, TRUNC, 3,
+                                                                 kWarpsPerCta, TIn, kCap>,
+                                      grid, 32 * kWarpsPerCta, 0, stream, p);
+            }
             return launch_pdl(
                 credit_forward_pipe_kernel<kItems, kVec16, TRUNC, fp.depth, kWarpsPerCta, TIn>,
                 grid, 32 * kWarpsPerCta, 0, stream, p);

@@ -659,11 +659,12 @@ __device__ __forceinline__ void warp_pipe_row(const Params &p, int64_t row, Scan
 // 9.17 / 8.96 / 9.43; fp16 TD(lambda) 7.40 / 7.60 / 7.50, GAE 10.89 / 10.74 / 10.43,
 // V-trace 11.89 / 12.36 / 12.27, Retrace 9.91 / 9.02 / 9.20; fused TD(lambda) 14.40 /
 // 14.53 / 14.55. The differences follow the register allocation of each kernel more
-// than the latency itself.
+// than the latency itself. The fp32 return's pipelined rows (rows of 513-960 steps)
+// take mode 2 as TD(lambda) does.
 template <Est E, typename TIn>
 __host__ __device__ constexpr int pipe_boot_mode()
 {
-    if (sizeof(TIn) == 4) return E == Est::kTdLambda ? 2 : 0;
+    if (sizeof(TIn) == 4) return (E == Est::kTdLambda || E == Est::kReturn) ? 2 : 0;
     if (E == Est::kVtrace || E == Est::kRetrace)
         return (E == Est::kVtrace && !std::is_same<TIn, uint16_t>::value) ? 0 : 1;
     if (E == Est::kTdLambda && !std::is_same<TIn, uint16_t>::value) return 0;

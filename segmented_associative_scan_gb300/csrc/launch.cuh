@@ -494,6 +494,18 @@ cudaError_t launch_estimator(const Params &p_in, int vec, cudaStream_t stream)
             return trunc ? launch_warp_pipe<E, kVec16, true, D>(p, stream)
                          : launch_warp_pipe<E, kVec16, false, D>(p, stream);
         }
+    } else if constexpr (E == Est::kReturn) {
+        // Rows of 513-960 steps that one wave of 7 CTAs of 4 warps per SM holds: the
+        // pipelined warp rows with two chunks in flight under that cap beat the CTA row,
+        // whose threads past the row's end idle. Measured on GB300, us per launch, CTA
+        // row vs pipelined rows at [4096, T]: T = 520 5.89 vs 5.24, 600 6.06 vs 5.40, 700
+        // 6.92 vs 6.13, 768 5.80 vs 5.17, 900 7.95 vs 7.53, 1000 7.79 vs 8.01, 1024 6.66
+        // vs 7.11; [2048, 600] 4.69 vs 4.36, [2048, 1024] 3.76 vs 5.14.
+        constexpr int kCap = 7;
+        if (path == Path::kCtaRows && one_row_per_cta(p.T) && p.T <= 960 && vec >= 1 &&
+            !p.host && (p.N + kWarpsPerCta - 1) / kWarpsPerCta <= (int64_t)kCap * sm_count())
+            return trunc ? launch_warp_pipe<E, kVec16, true, 2, float, kCap>(p, stream)
+                         : launch_warp_pipe<E, kVec16, false, 2, float, kCap>(p, stream);
     }
     // TD(lambda) keeps 128-bit access on a CTA row (measured 10.07 vs 10.16 us at
     // [4096, 1024]); it takes the CTA row only without 16-byte aligned rows now.

@@ -134,9 +134,10 @@ def test_wide_access_with_ragged_tails(kind, T):
 @pytest.mark.parametrize("T", [260, 264, 500, 512, 520, 768, 1000, 1016, 1024])
 def test_forward_pipelined_rows(N, T):
     """Rows of 257-1024 steps in 16-byte aligned rows: a warp per row walks its chunks of
-    256 steps from the first with the next chunk's loads in flight; a ragged last chunk is
+    256 steps from the first with the next chunks' loads in flight; a ragged last chunk is
     loaded plainly at the end. Episode ends planted on the last step of a chunk (the next
-    chunk starts afresh) and on the first step of one."""
+    chunk starts afresh) and on the first step of one. (fp32 rows that one wave of warps
+    holds keep three chunks in flight; more rows keep two: see the next test.)"""
     ro = sr.generic(N, T, seed=300 + 7 * N + T, p_term=0.01, p_trunc=0.01)
     for t in (255, 256, 511, 767):
         if t < T:
@@ -156,3 +157,15 @@ def test_forward_pipelined_layouts(T, ld_extra, offset):
     for kind in ("trace", "sum"):
         g, r = run_both(ro, kind, ld=T + ld_extra, offset=offset)
         assert_parity({"o": g}, {"o": r}, f"{kind} T={T} ld+{ld_extra} off={offset}")
+
+
+@pytest.mark.parametrize("N,T", [(2600, 1024), (3000, 1024), (4096, 600), (4256, 777),
+                                 (4400, 1024), (6000, 520)])
+def test_forward_pipelined_rows_by_grid_size(N, T):
+    """fp32 rows whose grid fills most of one wave of warps under the 7-CTA cap take three
+    chunks in flight ([3000, 1024], [4096, 600], [4256, 777]); fewer rows ([2600, 1024])
+    and more than one wave ([4400, 1024], [6000, 520]) two chunks and no cap."""
+    ro = sr.generic(N, T, seed=500 + N + T, p_term=0.01, p_trunc=0.01)
+    for kind in ("trace", "sum"):
+        g, r = run_both(ro, kind)
+        assert_parity({"o": g}, {"o": r}, f"{kind} N={N} T={T}")

@@ -125,3 +125,14 @@ def test_bootstrap_read_early_or_late(N, T, fmt):
         for est in ESTIMATORS:
             assert_parity(run_gpu(est, ro, {}, in_dtype=dtype), run_oracle(est, ro, {}),
                           f"{est} {fmt} N={N} T={T} {case}")
+
+
+@pytest.mark.parametrize("N", [37, 4096, 5000])
+@pytest.mark.parametrize("T", [513, 600, 768, 900, 960, 961, 1024])
+def test_fp32_return_rows_by_length(N, T):
+    """The fp32 discounted return on rows of 513-960 steps takes the pipelined warp rows
+    (two chunks in flight, 7 CTAs per SM) while one wave holds them, the CTA row
+    otherwise (longer rows, N = 5000): both against the oracle."""
+    ro = sr.generic(N, T, seed=9000 + N + T, p_term=0.01, p_trunc=0.01)
+    assert_parity(run_gpu("return", ro, {}), run_oracle("return", ro, {}),
+                  f"return N={N} T={T}")
