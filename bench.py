@@ -172,6 +172,9 @@ NCU_TRAFFIC = {
     (_H, "td_lambda_bf16", 4096, 1024, False): 38_079_744,
     (_H, "retrace_bf16", 4096, 1024, False): 56_065_920,
     (_H, "trace_bf16", 4096, 1024, False): 35_079_808,
+    (_H, "return", 4096, 600, False): 22_927_104,
+    (_H, "trace_fp16", 4096, 1024, False): 35_175_552,
+    (_H, "trace", 8192, 1024, False): 85_703_808,
 }
 
 
