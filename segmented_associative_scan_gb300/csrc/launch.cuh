@@ -232,7 +232,7 @@ template <Est E, typename TIn, bool MULTI = false>
 constexpr PipePrefetch pipe_prefetch()
 {
     if (MULTI) return {512, 3};
-    if (std::is_same<TIn, float>::value) return E == Est::kTdLambda ? PipePrefetch{512, 3}
+    if (std::is_same<TIn, float>::value) return E == Est::kTdLambda ? PipePrefetch{512, 2}
                                                                     : PipePrefetch{256, 0};
     if (E == Est::kGae || E == Est::kTdLambda) return {256, 0};
     if (E == Est::kReturn) return {1024, 0};
@@ -242,12 +242,24 @@ constexpr PipePrefetch pipe_prefetch()
     return {512, 3};
 }
 
+// fp32 TD(lambda), alone or fused, keeps its setting only on rows of whole chunks; a
+// row that starts with a ragged chunk takes (256, 0). Measured on GB300 at [4096, T], us
+// per launch, (256, 0) / (512, 0) / (512, 2) / (512, 3) / (768, 0): TD(lambda) T = 520
+// 7.01 / 6.98 / 6.97 / 6.99 / 6.97; 700 8.31 / 9.09 / 9.09 / 9.10 / 9.15; 900 10.20 /
+// 10.70 / 10.65 / 10.71 / 11.37; 1024 9.38 / 9.94 / 8.89 / 9.03 / 10.54; fused TD(lambda)
+// (256, 0) / (512, 2) / (512, 3): T = 700 12.16 / 12.76 / 12.79, 1024 14.76 / 15.42 /
+// 14.34. GAE takes (256, 0) at every one of these lengths (at 700: 11.63 against
+// 12.38-12.67 for the others); the 16-bit settings above were confirmed at T = 1024.
 template <Est E, typename TIn, bool MULTI = false>
 void set_pipe_prefetch(Params &p)
 {
     constexpr PipePrefetch pf = pipe_prefetch<E, TIn, MULTI>();
     p.pf_first = pf.first;
     p.pf_ahead = pf.ahead;
+    if (E == Est::kTdLambda && std::is_same<TIn, float>::value && p.T % (32 * kItems) != 0) {
+        p.pf_first = 256;
+        p.pf_ahead = 0;
+    }
 }
 
 // One row per warp, kItems steps per lane, DEPTH chunks' loads in flight ahead of the
